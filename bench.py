@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step over a paged BF16 KV cache on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+kv_append of every sequence's new token into its page slot, then paged decode
+attention (split-context pass + merge) for every sequence, per layer.
+
+Default workload: batch 256 x context 2048, 1 layer, 32 query / 8 KV heads,
+head_dim 64, 16-token pages, 32768 shuffled pages (1 GiB of BF16 K/V, larger
+than L2, so no flush is needed).  Smaller workloads (--config) flush L2 between
+steps by writing a buffer twice the L2 size.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job algorithmic HBM bytes per
+second (GB/s) with inputs resident; `e2e` is the same metric through the
+library's public calls with the step's inputs copied from pinned host memory and
+the output copied back inside the timed region.  `--impl reference` times the
+FP64 CPU oracle on the host cores instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged decode attention HBM GB/s and % of GB300 peak; sequence-layers/s"
+APPEND_BYTES_PER_TOKEN = 2 * 1024 * 2 + 4   # read K and V rows (1 KiB each), write them, read the slot
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny"], default="bandwidth")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    return p.parse_args()
+
+
+def make_workload(name: str):
+    from workloads import configs
+    return configs.CONFIGS[name]()
+
+
+def step_bytes(wl) -> tuple[int, int]:
+    """(attention bytes per layer, append bytes per layer) of one step."""
+    seqs_with_tokens = int(np.sum(wl.context_lens > 0))
+    return wl.algorithmic_bytes(), seqs_with_tokens * APPEND_BYTES_PER_TOKEN
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the split-context kernel from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    src = os.path.join(ROOT, "paged_kv_cache_180_gb300", "csrc", "decode_attention.cu")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("kernel_source_sha256") != sha:
+            return None
+        return rec.get("traffic_bytes_per_launch_full_workload")
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken every 100 ms while running."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        note = None
+        if not inside:  # timed region shorter than the sampling period: nearest sample
+            inside = [min(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))]
+            note = "timed region shorter than the 100 ms sampling period; nearest sample"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for _, p in inside if num(p[2]) is not None]
+        mx = [num(p[3]) for _, p in inside if num(p[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in inside:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": sorted(reasons), "samples": len(inside),
+               "power_w_max": max((num(p[4]) or 0.0) for _, p in inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_run(wl, threads: int, reps: int = 3):
+    """Times the FP64 oracle (as it stands) on the host: append of every token of the
+    sampled sequences into its own pool, then attention, threaded over sequences."""
+    import oracle
+    seqs = list(range(wl.num_seqs))
+    pool = oracle.Pool(wl.num_pages)
+    q = wl.q(0)
+    bt = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    lens = np.ascontiguousarray(wl.context_lens)
+    kv = {}
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for s, res in zip(seqs, ex.map(lambda s: wl.kv_tokens(s, 0), seqs)):
+            kv[s] = res
+    slots = {s: wl.slot_mapping(s, 0, 0, int(lens[s])) for s in seqs}
+
+    def one(s):
+        k, v = kv[s]
+        oracle.kv_append(pool, k, v, slots[s])
+        out, err = oracle.paged_decode_attention(pool, q[s:s + 1], bt[s:s + 1], lens[s:s + 1], wl.scale,
+                                                 wl.max_context)
+        return err
+
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            errs = list(ex.map(one, seqs))
+        times.append(time.perf_counter() - t0)
+        assert not any(errs)
+    return statistics.median(times), len(seqs)
+
+
+def cpu_baseline(wl):
+    threads = os.cpu_count() or 1
+    t, nseq = cpu_oracle_run(wl, threads)
+    attn, app = step_bytes(wl)
+    return {"value": round((attn + app) / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"the whole {wl.name} step ({nseq} sequences, 1 layer: append of every token into the "
+                      f"oracle's own pool + FP64 attention), median of 3 passes, threaded over sequences",
+            "seconds_per_step": round(t, 4), "seq_layers_per_s": round(nseq / t, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = make_workload(args.config)
+    steps = args.steps if args.steps is not None else 3
+    warmup = args.warmup if args.warmup is not None else 1
+    threads = os.cpu_count() or 1
+    import oracle
+    oracle.build()
+    for _ in range(warmup):
+        cpu_oracle_run(wl, threads, reps=1)
+    times = [cpu_oracle_run(wl, threads, reps=1)[0] for _ in range(steps)]
+    t = sum(times) / len(times)
+    attn, app = step_bytes(wl)
+    value = (attn + app) / t / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 K/V/q)",
+            "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "layers": wl.num_layers,
+                       "context": "per-sequence lengths of the workload", "q_heads": 32, "kv_heads": 8,
+                       "head_dim": 64, "page_tokens": 16, "parallelism": "host threads", "l2": "n/a (CPU)"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: the whole {wl.name} step (append + FP64 attention of every "
+                                       f"sequence) on the host cores"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "seq_layers_per_s": round(wl.num_seqs * wl.num_layers / t, 2)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+
+    wl = make_workload(args.config)
+    L = wl.num_layers
+    steps = args.steps if args.steps is not None else (10000 if wl.name == "bandwidth" else 2000)
+    warmup = args.warmup if args.warmup is not None else 20
+
+    # ---- resident state: the pool holds every token but each sequence's decode token ----
+    pool = pkv.KVPool(wl.num_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for layer in range(L):
+        k, v, slots = torch_gen.workload_kv(wl, layer, dev, upto_offset=1)
+        if slots.numel():
+            pkv.kv_append(pool, k, v, slots, status)
+        del k, v, slots
+    bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables)).to(dev)
+    lens = torch.from_numpy(wl.context_lens).to(dev)
+    q = [torch_gen.workload_q(wl, layer, dev) for layer in range(L)]
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    dec = [tuple(to_dev(a) for a in wl.decode_tokens(layer)) for layer in range(L)]
+    out = torch.empty(wl.num_seqs, 32, 64, dtype=torch.float32, device=dev)
+    ws = torch.empty(pkv.decode_workspace_bytes(wl.num_seqs), dtype=torch.uint8, device=dev)
+    blocks = wl.max_blocks
+    stride = L * blocks
+    stream = torch.cuda.current_stream(dev)
+    ctas, attn_launches = pkv.decode_plan(wl.num_seqs, wl.max_context)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = wl.num_pages * 32768
+    flush = None
+    if pool_bytes < 2 * l2:
+        flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+
+    def step(e_marks=None):
+        for layer in range(L):
+            kn, vn, sn = dec[layer]
+            if e_marks is not None:
+                e_marks[0].record(stream)
+            pkv.kv_append(pool, kn, vn, sn, status)
+            if e_marks is not None:
+                e_marks[1].record(stream)
+            pkv.paged_decode_attention(pool, out, q[layer], bt.view(-1)[layer * blocks:], stride, lens,
+                                       wl.max_context, wl.scale, ws, status)
+            if e_marks is not None:
+                e_marks[2].record(stream)
+                e_marks = e_marks[3:]
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- timed region: device time of every step, per-kernel events on the launching stream ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    append_ms, attn_ms, step_ms = [], [], []
+    for i in range(steps):
+        tot = 0.0
+        for layer in range(L):
+            e0, e1, e2 = ev[i][3 * layer:3 * layer + 3]
+            a, b = e0.elapsed_time(e1), e1.elapsed_time(e2)
+            append_ms.append(a)
+            attn_ms.append(b)
+            tot += a + b
+        step_ms.append(tot)
+    ms = sum(step_ms) / steps
+    t_dev = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_dev, op=dist.ReduceOp.MAX)
+    ms_max = float(t_dev.item())
+
+    attn_b, app_b = step_bytes(wl)
+    bytes_step = (attn_b + app_b) * L
+    value = world * bytes_step / (ms_max * 1e-3) / 1e9
+    attn_avg_s = (sum(attn_ms) / len(attn_ms)) * 1e-3
+    achieved = attn_b / attn_avg_s / 1e9
+    peak, peak_kind = measured_peak()
+
+    # ---- end to end through the public calls with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_q = [pin(x) for x in q]
+        h_dec = [tuple(pin(x) for x in d) for d in dec]
+        h_bt, h_lens = pin(bt), pin(lens)
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d_q = [torch.empty_like(x) for x in q]
+        d_dec = [tuple(torch.empty_like(x) for x in d) for d in dec]
+        d_bt, d_lens = torch.empty_like(bt), torch.empty_like(lens)
+        h2d = sum(x.numel() * x.element_size() for x in h_q) + sum(
+            x.numel() * x.element_size() for d in h_dec for x in d) + h_bt.numel() * 4 + h_lens.numel() * 4
+        d2h = h_out.numel() * 4 * L
+
+        def e2e_step():
+            d_bt.copy_(h_bt, non_blocking=True)
+            d_lens.copy_(h_lens, non_blocking=True)
+            for layer in range(L):
+                d_q[layer].copy_(h_q[layer], non_blocking=True)
+                for dst, src in zip(d_dec[layer], h_dec[layer]):
+                    dst.copy_(src, non_blocking=True)
+                kn, vn, sn = d_dec[layer]
+                pkv.kv_append(pool, kn, vn, sn, status)
+                pkv.paged_decode_attention(pool, out, d_q[layer], d_bt.view(-1)[layer * blocks:], stride, d_lens,
+                                           wl.max_context, wl.scale, ws, status)
+                h_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        e2e_steps = max(3, min(steps, 200))
+        for _ in range(3):
+            e2e_step()
+        ts = []
+        for _ in range(e2e_steps):
+            if flush is not None:
+                flush.zero_()
+                torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            ts.append(time.perf_counter() - t0)
+        t_e2e = torch.tensor([sum(ts) / len(ts)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+        e2e = {"value": round(world * bytes_step / float(t_e2e.item()) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(float(t_e2e.item()) * 1e3, 4),
+               "how": "host wall clock per step: pinned H2D of q, new K/V, slots, tables, lengths; append + "
+                      "attention; D2H of the output; stream synchronize"}
+
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/out", "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "layers": L,
+                       "context_lens": ("2048 each" if wl.name == "bandwidth" else "per workload"),
+                       "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
+                       "pool_pages": wl.num_pages, "parallelism": f"replicas x{world}",
+                       "l2": ("inputs larger than L2 (1 GiB pool)" if flush is None else
+                              "L2 flushed between steps (write of 2x L2)"),
+                       "split_ctas": ctas},
+            "seq_layers_per_s": round(world * wl.num_seqs * L / (ms_max * 1e-3), 1),
+            "pct_of_peak": {"measured": round(100 * value / world / peak, 2),
+                            "nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
+                         "kernel": "paged_decode_attention call (split-context pass + merge)",
+                         "algorithmic_bytes_per_launch": attn_b, "avg_launch_us": round(attn_avg_s * 1e6, 3),
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s"},
+            "kernel_us": {"kv_append": round(1e3 * sum(append_ms) / len(append_ms), 3),
+                          "paged_decode_attention": round(1e3 * sum(attn_ms) / len(attn_ms), 3)},
+            "clocks": clocks,
+            "gpu_launches": steps * L * (1 + attn_launches),
+            "e2e": e2e,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    # CPU baseline (the oracle as it stands), rank 0 at N=1 only, on the machine's host cores.
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * pkv.h - C ABI of the paged KV-cache decode library for GB300 (sm_103a).
+ *
+ * Single-token decode attention over a paged BF16 KV cache.  Each sequence's K
+ * and V live in physical pages of a shared pool, reached through a block table
+ * per (sequence, layer); decode appends one token's K/V into its slot, then
+ * every query head attends over the sequence's cached tokens with an FP32
+ * online softmax, without gathering a contiguous prefix or storing scores.
+ *
+ * Sources (web pages on the method):
+ *  - "6 Hours of YouTube ... LLM Inference" (samir-vllm README), section "What
+ *    works so far": one shared BF16 page pool, a block table per sequence and
+ *    layer, 16 tokens of K and V per page, decode appends one token at its
+ *    absolute position, paged decode attention with an FP32 online softmax
+ *    that streams each sequence's pages; section "Current scope": 2048-token
+ *    context, 128 MiB default pool.
+ *  - "tiny-vllm part 3: the prefill path", section "Distributing K/V into paged
+ *    blocks" (block = token / 16, block table lookup, -1 = unassigned, K at the
+ *    block start and V at a fixed offset); section "Per-head attention scores
+ *    and GQA" (32 query heads share 8 K/V heads, query head h reads K/V head
+ *    h / 4, scale 1/sqrt(64)); section "causalMask and online softmax" (the
+ *    merge rule of two partial softmax states: m = max(ma, mb),
+ *    d = da*exp(ma - m) + db*exp(mb - m)).
+ *
+ * Conventions for every entry point:
+ *  - Buffers are owned by the caller.  The library never allocates, frees or
+ *    synchronises; device work is enqueued on the caller's stream.
+ *  - "device" pointers must be CUDA device (or managed) memory of the current
+ *    device; "host" pointers are ordinary host memory.
+ *  - bf16 values are passed as raw 16-bit patterns (bfloat16, i.e. the upper
+ *    half of an IEEE binary32).
+ *  - Host-checkable faults return a negative PKV_ERR_* code and enqueue
+ *    nothing.  Faults only the device can see (bad slots, context lengths or
+ *    block-table entries) are OR-ed as PKV_DEV_* bits into *device_status when
+ *    that pointer is non-null; the host never reads device memory.
+ *  - `stream` is a cudaStream_t (0 = legacy default stream).
+ *
+ * Supported geometry in this build: page_tokens 16, head_dim 64, 8 K/V heads,
+ * 32 query heads (group 4).  Other values are rejected with
+ * PKV_ERR_UNSUPPORTED.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (host side) ------------------------------------------ */
+#define PKV_OK 0
+#define PKV_ERR_NULL (-1)          /* a required pointer is null */
+#define PKV_ERR_SHAPE (-2)         /* a size or count is out of range */
+#define PKV_ERR_UNSUPPORTED (-3)   /* geometry this build does not compile */
+#define PKV_ERR_ALIGN (-4)         /* pointer or stride not 16-byte aligned */
+#define PKV_ERR_SCALE (-5)         /* scale is not finite */
+#define PKV_ERR_WORKSPACE (-6)     /* workspace smaller than pkv_decode_workspace_bytes() */
+#define PKV_ERR_LAUNCH (-7)        /* the CUDA runtime refused a kernel launch */
+#define PKV_ERR_CUDA (-8)          /* another CUDA runtime call failed */
+#define PKV_ERR_EXCEEDS_POOL (-9)  /* scheduler: a request's page budget exceeds the whole pool */
+#define PKV_ERR_NO_PAGE (-10)      /* allocator: no free page */
+#define PKV_ERR_STATE (-11)        /* scheduler/allocator used out of order */
+
+/* ---- device status bits (OR-ed into *device_status) --------------------- */
+#define PKV_DEV_BAD_SLOT 1u        /* kv_append: slot >= num_pages * page_tokens; token not written */
+#define PKV_DEV_BAD_CONTEXT 2u     /* context_lens[s] < 0 or > max_context; row s of out is zeros */
+#define PKV_DEV_BAD_PAGE 4u        /* block-table entry outside [0, num_pages) inside the context;
+                                      that page's tokens are left out of the softmax */
+#define PKV_DEV_TIMEOUT 8u         /* an internal pipeline wait gave up (about 2 s); the CTA stopped */
+
+/*
+ * Pool descriptor (plain data; copying it is free).
+ *
+ * K element (page p, kv_head g, row r, dim d) is the bf16 at
+ *     k_base + p * page_stride_bytes + ((g * page_tokens + r) * head_dim + d) * 2
+ * and V likewise from v_base.  In the default interleaved buffer
+ * (pkv_kv_pool_bytes) a page is [K | V][kv_head][row][dim]: K in the first
+ * half and V at +num_kv_heads*page_tokens*head_dim*2 bytes (16 KiB for the
+ * supported geometry), page stride 32 KiB.  Slot s names page
+ * s / page_tokens, row s % page_tokens.
+ */
+typedef struct pkv_pool {
+    void *k_base;               /* device */
+    void *v_base;               /* device */
+    int64_t page_stride_bytes;  /* bytes between consecutive pages (same for K and V) */
+    int32_t num_pages;
+    int32_t page_tokens;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} pkv_pool;
+
+/* Bytes of one interleaved pool buffer of num_pages pages ([page][K|V][kv_head][row][dim] bf16). */
+size_t pkv_kv_pool_bytes(int num_pages, int page_tokens, int num_kv_heads, int head_dim);
+
+/*
+ * pkv_kv_pool_create - describe caller-owned pool memory (no allocation, no device work).
+ *   k_pool, v_pool     device; for the interleaved buffer pass v_pool = k_pool + half a page
+ *                      and page_stride_bytes = 0 (meaning: 2 * half page).
+ *   page_stride_bytes  bytes between pages, >= half a page, multiple of 16 (0 = interleaved default)
+ *   out                host; receives the descriptor.
+ * Returns PKV_OK, PKV_ERR_NULL, PKV_ERR_SHAPE, PKV_ERR_ALIGN (pointers or stride not
+ * 16-byte aligned) or PKV_ERR_UNSUPPORTED.
+ * Cited: samir-vllm README "What works so far" (shared BF16 page pool, 16-token pages).
+ */
+int pkv_kv_pool_create(void *k_pool, void *v_pool, int64_t page_stride_bytes, int num_pages,
+                       int page_tokens, int num_kv_heads, int head_dim, pkv_pool *out);
+
+/*
+ * pkv_kv_append - scatter the K/V of num_tokens new tokens into their slots (bit copy).
+ *   pool          host; descriptor from pkv_kv_pool_create.
+ *   k_new, v_new  device; bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned.
+ *   slot_mapping  device; int32 [num_tokens]; slot = page * page_tokens + row; a negative slot
+ *                 is padding and is skipped; a slot >= num_pages * page_tokens is skipped and
+ *                 sets PKV_DEV_BAD_SLOT.
+ *   device_status device int32, nullable.
+ * Two tokens naming the same slot race (either may win).  num_tokens = 0 enqueues nothing.
+ * Cited: samir-vllm README "What works so far" (decode appends one new token at its absolute
+ * position); tiny-vllm part 3, "Distributing K/V into paged blocks" (page/row of a token,
+ * K and V copied into the block).
+ */
+int pkv_kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                  int num_tokens, int32_t *device_status, void *stream);
+
+/*
+ * Workspace bytes pkv_paged_decode_attention needs for num_seqs sequences (holds
+ * split-context partial softmax states; no need to clear it).  0 on bad arguments.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
+
+/*
+ * pkv_paged_decode_attention - one decode step of attention for num_seqs sequences.
+ *
+ *   out[s][h][:] = sum_{t < ctx_s} w_t V_t[h / group][:],
+ *   w = softmax_t( scale * q[s][h] . K_t[h / group] ),   group = num_q_heads / num_kv_heads,
+ *   K_t, V_t read from page block_tables[s * block_table_stride + t / page_tokens],
+ *   row t % page_tokens.
+ *
+ *   pool               host; descriptor.
+ *   out                device; float32 [num_seqs][num_q_heads][head_dim], 8-byte aligned.
+ *   q                  device; bf16 [num_seqs][num_q_heads][head_dim], 16-byte aligned.
+ *   block_tables       device; int32; row s starts at s * block_table_stride and holds at least
+ *                      ceil(max_context / page_tokens) entries (a multi-layer table
+ *                      [seq][layer][blocks] is passed as base + layer * blocks with
+ *                      stride layers * blocks).
+ *   context_lens       device; int32 [num_seqs]; tokens to attend (the new token included).
+ *                      0 gives a zero output row.
+ *   max_context        host bound on every context_lens[s] (chooses the work split; a larger
+ *                      length sets PKV_DEV_BAD_CONTEXT and zeroes that row).
+ *   scale              softmax scale (1/sqrt(head_dim) for the pages' model).
+ *   workspace          device, >= pkv_decode_workspace_bytes(num_seqs, ...), 16-byte aligned.
+ *   device_status      device int32, nullable.
+ * Enqueues one kernel, or two (a split-context pass and a merge) when the work is
+ * split across CTAs.  Calls sharing a workspace must not overlap on the GPU.
+ * Returns PKV_OK or a negative PKV_ERR_* code (then nothing was enqueued).
+ * Cited: samir-vllm README "What works so far" (direct paged decode attention, FP32
+ * online softmax, no contiguous gather, no stored scores; separate page maps and
+ * lengths per sequence); tiny-vllm part 3, "Per-head attention scores and GQA" and
+ * "causalMask and online softmax" (GQA mapping, scale, softmax merge rule).
+ */
+int pkv_paged_decode_attention(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                               const int32_t *block_tables, int64_t block_table_stride,
+                               const int32_t *context_lens, int num_seqs, int max_context, float scale,
+                               void *workspace, size_t workspace_bytes, int32_t *device_status,
+                               void *stream);
+
+/*
+ * Same as pkv_paged_decode_attention with the number of CTAs of the split-context pass
+ * fixed by the caller (1 .. pkv_decode_max_ctas(); 0 = automatic).  The result must not
+ * depend on it beyond FP32 rounding; tests sweep it.
+ */
+int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                    const int32_t *block_tables, int64_t block_table_stride,
+                                    const int32_t *context_lens, int num_seqs, int max_context,
+                                    float scale, void *workspace, size_t workspace_bytes,
+                                    int32_t *device_status, int num_ctas, void *stream);
+
+/* Largest CTA count the split-context pass may use (sizes the workspace). */
+int pkv_decode_max_ctas(void);
+
+/*
+ * Launch plan of pkv_paged_decode_attention on the current device: CTAs of the
+ * split-context pass and kernel launches per call.  Returns PKV_OK or an error.
+ */
+int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches);
+
+/* Short English text for a PKV_ERR_* code or PKV_OK. */
+const char *pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,166 @@
+"""Thin Python binding of the C ABI in ``include/pkv.h`` (argument marshalling only).
+
+Every step of the decode path runs in the CUDA kernels of ``libpkv.so``; this
+module only turns tensors into pointers and sizes, passes the current CUDA
+stream, and raises on a negative status.  There is no CPU fallback: if the
+library is missing the import fails.
+
+Function names follow the C entry points without their ``pkv_`` prefix.
+PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_180_gb300.build` "
+                      "(the CUDA path has no fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PKV_OK = 0
+DEV_BAD_SLOT = 1
+DEV_BAD_CONTEXT = 2
+DEV_BAD_PAGE = 4
+DEV_TIMEOUT = 8
+
+
+class PkvPool(ctypes.Structure):
+    """Mirror of ``pkv_pool``."""
+    _fields_ = [("k_base", ctypes.c_void_p), ("v_base", ctypes.c_void_p), ("page_stride_bytes", ctypes.c_int64),
+                ("num_pages", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_P, _I, _L, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_PP = ctypes.POINTER(PkvPool)
+
+EXPORTS = {
+    # name: (restype, argtypes)
+    "pkv_kv_pool_bytes": (_Z, [_I, _I, _I, _I]),
+    "pkv_kv_pool_create": (_I, [_P, _P, _L, _I, _I, _I, _I, _PP]),
+    "pkv_kv_append": (_I, [_PP, _P, _P, _P, _I, _P, _P]),
+    "pkv_decode_workspace_bytes": (_Z, [_I, _I, _I]),
+    "pkv_paged_decode_attention": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, _P]),
+    "pkv_paged_decode_attention_ctas": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, _I, _P]),
+    "pkv_decode_max_ctas": (_I, []),
+    "pkv_decode_plan": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "pkv_status_string": (ctypes.c_char_p, [_I]),
+}
+
+for _name, (_res, _args) in EXPORTS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class PkvError(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _check(where: str, rc: int) -> None:
+    if rc != PKV_OK:
+        raise PkvError(where, rc)
+
+
+def status_string(code: int) -> str:
+    return _lib.pkv_status_string(int(code)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+def kv_pool_bytes(num_pages: int, page_tokens: int = 16, num_kv_heads: int = 8, head_dim: int = 64) -> int:
+    return int(_lib.pkv_kv_pool_bytes(num_pages, page_tokens, num_kv_heads, head_dim))
+
+
+def kv_pool_create(k_pool: torch.Tensor | int, v_pool: torch.Tensor | int, page_stride_bytes: int, num_pages: int,
+                   page_tokens: int = 16, num_kv_heads: int = 8, head_dim: int = 64) -> PkvPool:
+    """Descriptor for caller-owned pool memory (tensors or raw device addresses)."""
+    kp = k_pool if isinstance(k_pool, int) else _ptr(k_pool)
+    vp = v_pool if isinstance(v_pool, int) else _ptr(v_pool)
+    desc = PkvPool()
+    _check("pkv_kv_pool_create", _lib.pkv_kv_pool_create(kp, vp, page_stride_bytes, num_pages, page_tokens,
+                                                         num_kv_heads, head_dim, ctypes.byref(desc)))
+    return desc
+
+
+class KVPool:
+    """One interleaved pool buffer ([page][K|V][kv_head][row][dim] bf16) owned by a torch tensor."""
+
+    def __init__(self, num_pages: int, page_tokens: int = 16, num_kv_heads: int = 8, head_dim: int = 64,
+                 device="cuda", buffer: torch.Tensor | None = None):
+        nbytes = kv_pool_bytes(num_pages, page_tokens, num_kv_heads, head_dim)
+        if buffer is None:
+            buffer = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device)
+        assert buffer.numel() * buffer.element_size() >= nbytes
+        self.buffer = buffer
+        self.num_pages, self.page_tokens = num_pages, page_tokens
+        self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
+        half = num_kv_heads * page_tokens * head_dim * 2
+        base = _ptr(buffer)
+        self.desc = kv_pool_create(base, base + half, 2 * half, num_pages, page_tokens, num_kv_heads, head_dim)
+
+    def view(self) -> torch.Tensor:
+        """The pool as [num_pages, 2, num_kv_heads, page_tokens, head_dim] bf16."""
+        return self.buffer[: self.num_pages * 2 * self.num_kv_heads * self.page_tokens * self.head_dim].view(
+            self.num_pages, 2, self.num_kv_heads, self.page_tokens, self.head_dim)
+
+
+def kv_append(pool: KVPool | PkvPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+              status: torch.Tensor | None = None, stream=None) -> None:
+    desc = pool.desc if isinstance(pool, KVPool) else pool
+    n = int(slot_mapping.shape[0])
+    _check("pkv_kv_append", _lib.pkv_kv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                               n, _ptr(status), _stream(stream)))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int = 32, head_dim: int = 64) -> int:
+    return int(_lib.pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim))
+
+
+def decode_max_ctas() -> int:
+    return int(_lib.pkv_decode_max_ctas())
+
+
+def decode_plan(num_seqs: int, max_context: int) -> tuple[int, int]:
+    g, n = _I(0), _I(0)
+    _check("pkv_decode_plan", _lib.pkv_decode_plan(num_seqs, max_context, ctypes.byref(g), ctypes.byref(n)))
+    return g.value, n.value
+
+
+def paged_decode_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.Tensor, block_tables: torch.Tensor,
+                           block_table_stride: int, context_lens: torch.Tensor, max_context: int, scale: float,
+                           workspace: torch.Tensor, status: torch.Tensor | None = None, num_ctas: int = 0,
+                           stream=None) -> None:
+    """out[s, h, :] = softmax(scale * q[s, h] . K[h // group]) V over the cached tokens of sequence s."""
+    desc = pool.desc if isinstance(pool, KVPool) else pool
+    num_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if num_ctas:
+        rc = _lib.pkv_paged_decode_attention_ctas(ctypes.byref(desc), _ptr(out), _ptr(q), num_q_heads,
+                                                  _ptr(block_tables), block_table_stride, _ptr(context_lens),
+                                                  num_seqs, max_context, scale, _ptr(workspace), ws_bytes,
+                                                  _ptr(status), num_ctas, _stream(stream))
+    else:
+        rc = _lib.pkv_paged_decode_attention(ctypes.byref(desc), _ptr(out), _ptr(q), num_q_heads,
+                                             _ptr(block_tables), block_table_stride, _ptr(context_lens),
+                                             num_seqs, max_context, scale, _ptr(workspace), ws_bytes,
+                                             _ptr(status), _stream(stream))
+    _check("pkv_paged_decode_attention", rc)

@@ -1,0 +1,562 @@
+// Paged decode attention: one query token per sequence attends over that
+// sequence's cached K/V, read page by page through its block table, with an FP32
+// online softmax and grouped-query heads.
+//
+// What is computed (samir-vllm README, "What works so far": direct paged decode
+// attention with FP32 online softmax, each query head streams its sequence's
+// cached pages, no contiguous gather, no stored scores; "tiny-vllm part 3",
+// "Per-head attention scores and GQA": query head h uses K/V head h / 4, scale
+// 1/sqrt(64); same page, "causalMask and online softmax": two partial softmax
+// states (m, d) combine as m = max(ma, mb), d = da e^(ma-m) + db e^(mb-m) - here
+// extended with the weighted-V accumulator so that partial results over disjoint
+// token ranges merge exactly):
+//
+//   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t[h/4]) V_t[h/4]
+//
+// GB300 design
+//  * Work split: the pages of all sequences form one list (sequence-major); the
+//    grid has G CTAs (a multiple of the SM count) and CTA c takes pages
+//    [c*T/G, (c+1)*T/G) of the T pages in the list, so every CTA streams the
+//    same number of bytes whatever the mix of context lengths.  A sequence
+//    covered by one CTA is written out directly; a sequence cut across CTAs
+//    leaves one partial state (m, l, acc) per CTA in the workspace, combined by
+//    the merge kernel.  The partial of (CTA c, sequence s) lives in slot c + s,
+//    unique because the (c, s) pairs of the list form a monotone staircase.
+//  * Staging: one producer thread streams whole pages (16 KiB of K, 16 KiB of V,
+//    contiguous in the pool) with 1-D bulk TMA copies into a ring of shared
+//    memory stages guarded by mbarriers; eight consumer warps (one per K/V head)
+//    read each page once from shared memory and serve all four query heads of
+//    their group from that single read.
+//  * Scores: lane (t4, c) of a warp holds q[8c .. 8c+7] of the four query heads
+//    (pre-multiplied by scale*log2(e), so the softmax runs on exp2); for
+//    tokens t = 4j + t4 it dots a 16-byte K chunk with packed FP32x2 FMAs and
+//    reduces across the eight chunk lanes with a transposing butterfly that
+//    leaves each lane one (token, head) score.
+//  * Softmax: running max and sum per head with warp shuffles; probabilities of a
+//    page go through 512 B of shared memory to the PV lanes.
+//  * PV: lane owns dims (2*lane, 2*lane+1) of the four heads and accumulates
+//    p * V with packed FMAs; V rows are read as 128 contiguous bytes per warp.
+//  * Every mbarrier wait is bounded (about 2 s); on expiry the CTA reports
+//    PKV_DEV_TIMEOUT and stops, after draining its outstanding copies.
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+
+#include "host_common.h"
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = kKvHeads;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxCtas = 1024;
+constexpr int kCtasPerSm = 2;
+constexpr int kMinPagesPerCta = 2;
+constexpr int kMergeThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+  const uint8_t *k_base;
+  const uint8_t *v_base;
+  long long page_stride;
+  int num_pages;
+  const uint4 *q;  // [num_seqs][32][64] bf16, 8 uint4 per head
+  float *out;      // [num_seqs][32][64]
+  const int32_t *block_tables;
+  long long bt_stride;
+  const int32_t *context_lens;
+  int num_seqs;
+  int max_context;
+  float scale_log2;  // scale * log2(e)
+  float *part_acc;   // [kMaxCtas + num_seqs][32][64]
+  float2 *part_ml;   // [kMaxCtas + num_seqs][32]  (running max in log2 units, sum)
+  int2 *seq_info;    // [num_seqs]  (first CTA, last CTA) touching the sequence
+  long long *meta;   // [2]: total pages T and CTA count G of the last split pass
+  int32_t *status;
+};
+
+struct __align__(128) Smem {
+  uint8_t kv[kStages][2][kHalfPageBytes];
+  float2 pbuf[kConsumerWarps][kPageTokens][kGroup];  // (p, p) pairs per (token, head)
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int stage_ok[kStages];
+  long long warp_sums[32];
+  long long total_pages;
+  long long seq0_first;  // global index of the first page of seq0
+  int seq0;
+  int found;
+};
+
+__device__ __forceinline__ int seq_pages(int ctx, int max_context) {
+  return (ctx > 0 && ctx <= max_context) ? (ctx + kPageTokens - 1) / kPageTokens : 0;
+}
+
+// Inclusive block-wide prefix sum (all kThreads threads must call).
+__device__ long long block_inclusive_scan(long long v, Smem &sm, long long *block_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm.warp_sums[warp] = x;
+  __syncthreads();
+  long long before = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const long long ws = sm.warp_sums[w];
+    if (w < warp) before += ws;
+    total += ws;
+  }
+  __syncthreads();
+  *block_total = total;
+  return x + before;
+}
+
+// CTA that owns global page p when T pages are split over G CTAs.
+__device__ __forceinline__ int cta_of_page(long long p, long long T, int G) {
+  return int(((p + 1) * G - 1) / T);
+}
+
+// Walk over the (sequence, local page) pairs of a CTA's page range.
+struct Walk {
+  int s, lp, n, ctx;
+  __device__ void next(const DecodeArgs &a) {
+    if (++lp < n) return;
+    lp = 0;
+    do {
+      ++s;
+      ctx = (s < a.num_seqs) ? __ldg(a.context_lens + s) : 1;
+      n = seq_pages(ctx, a.max_context);
+    } while (n == 0 && s < a.num_seqs);
+  }
+};
+
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int s, int g, int c, float (&qf)[kGroup][8]) {
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h) {
+    const uint4 w = __ldg(a.q + ((long long)s * kQHeads + g * kGroup + h) * 8 + c);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qf[h][2 * i] = bf16_lo(ws[i]) * a.scale_log2;
+      qf[h][2 * i + 1] = bf16_hi(ws[i]) * a.scale_log2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kConsumerWarps);
+    }
+    sm.found = 0;
+    mbar_init_fence();
+  }
+
+  // ---- total pages T, and this CTA's range [pa, pb) ----
+  long long mine = 0;
+  for (int i = tid; i < a.num_seqs; i += kThreads) {
+    const int c = __ldg(a.context_lens + i);
+    mine += seq_pages(c, a.max_context);
+    if (cta == 0 && (c < 0 || c > a.max_context)) report(a.status, PKV_DEV_BAD_CONTEXT);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) sm.warp_sums[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    long long t = 0;
+    for (int w = 0; w < kThreads / 32; ++w) t += sm.warp_sums[w];
+    sm.total_pages = t;
+    if (cta == 0) {
+      a.meta[0] = t;
+      a.meta[1] = G;
+    }
+  }
+  __syncthreads();
+  const long long T = sm.total_pages;
+  const long long pa = (long long)cta * T / G, pb = (long long)(cta + 1) * T / G;
+  if (pa >= pb) return;  // nothing assigned (uniform across the CTA)
+
+  // ---- first sequence of the range ----
+  long long running = 0;
+  for (int base = 0; base < a.num_seqs; base += kThreads) {
+    const int i = base + tid;
+    const int v = (i < a.num_seqs) ? seq_pages(__ldg(a.context_lens + i), a.max_context) : 0;
+    long long chunk_total;
+    const long long incl = block_inclusive_scan(v, sm, &chunk_total) + running;
+    if (v > 0 && incl - v <= pa && pa < incl) {
+      sm.seq0 = i;
+      sm.seq0_first = incl - v;
+      sm.found = 1;
+    }
+    __syncthreads();
+    if (sm.found) break;
+    running += chunk_total;
+  }
+  const long long count = pb - pa;
+
+  Walk w;
+  w.s = sm.seq0;
+  w.ctx = __ldg(a.context_lens + w.s);
+  w.n = seq_pages(w.ctx, a.max_context);
+  w.lp = int(pa - sm.seq0_first);
+
+  if (warp == kConsumerWarps) {
+    // ================= producer: one thread streams pages =================
+    if (lane != 0) return;
+    const uint64_t policy = policy_evict_first();
+    long long issued = 0;
+    bool ok = true;
+    for (long long i = 0; i < count; ++i) {
+      const int st = int(i % kStages);
+      const uint32_t round = uint32_t(i / kStages);
+      if (i >= kStages && !mbar_wait(&sm.empty[st], (round - 1) & 1)) {
+        report(a.status, PKV_DEV_TIMEOUT);
+        ok = false;
+        break;
+      }
+      const int page = __ldg(a.block_tables + (long long)w.s * a.bt_stride + w.lp);
+      if (page >= 0 && page < a.num_pages) {
+        sm.stage_ok[st] = 1;
+        mbar_arrive_expect_tx(&sm.full[st], 2 * kHalfPageBytes);
+        bulk_load(sm.kv[st][0], a.k_base + (long long)page * a.page_stride, kHalfPageBytes, &sm.full[st], policy);
+        bulk_load(sm.kv[st][1], a.v_base + (long long)page * a.page_stride, kHalfPageBytes, &sm.full[st], policy);
+      } else {
+        report(a.status, PKV_DEV_BAD_PAGE);
+        sm.stage_ok[st] = 0;
+        mbar_arrive(&sm.full[st]);
+      }
+      ++issued;
+      if (i + 1 < count) w.next(a);
+    }
+    if (!ok) {
+      // Drain: wait (bounded) for the copies still landing in the stages that
+      // were issued but possibly not consumed, so none outlives the CTA.
+      const long long first = issued > kStages ? issued - kStages : 0;
+      for (long long i = first; i < issued; ++i)
+        mbar_wait(&sm.full[int(i % kStages)], uint32_t(i / kStages) & 1);
+    }
+    return;
+  }
+
+  // ================= consumers: warp g serves K/V head g =================
+  const int g = warp;
+  const int t4 = lane >> 3, c = lane & 7;
+  const int hh = c >> 1;  // head (within the group) whose score this lane ends up holding
+  float qf[kGroup][8];
+  load_q(a, w.s, g, c, qf);
+  float m_run = -INFINITY, l_run = 0.f;
+  float2 acc[kGroup];
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h) acc[h] = make_float2(0.f, 0.f);
+  bool has_first = (w.lp == 0);
+  long long gfirst = pa - w.lp;  // global index of the first page of the current sequence
+
+  for (long long i = 0; i < count; ++i) {
+    const int st = int(i % kStages);
+    if (!mbar_wait(&sm.full[st], uint32_t(i / kStages) & 1)) {
+      report(a.status, PKV_DEV_TIMEOUT);
+      return;
+    }
+    const int valid = min(kPageTokens, w.ctx - w.lp * kPageTokens);
+    if (sm.stage_ok[st]) {
+      const uint8_t *Kg = sm.kv[st][0] + g * (kPageTokens * kRowBytes);
+      const uint8_t *Vg = sm.kv[st][1] + g * (kPageTokens * kRowBytes);
+      // ---- scores: lane ends with s[j] = score(token 4j+t4, head hh) in log2 units ----
+      float s[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int t = 4 * j + t4;
+        const uint4 kw = *reinterpret_cast<const uint4 *>(Kg + t * kRowBytes + c * 16);
+        const uint32_t ws[4] = {kw.x, kw.y, kw.z, kw.w};
+        float part[kGroup];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2)
+            d2 = __ffma2_rn(make_float2(qf[h][2 * q2], qf[h][2 * q2 + 1]),
+                            make_float2(bf16_lo(ws[q2]), bf16_hi(ws[q2])), d2);
+          part[h] = d2.x + d2.y;
+        }
+        // transposing butterfly over the 8 chunk lanes (xor 4, 2, 1)
+        const bool b2 = (c >> 2) & 1, b1 = (c >> 1) & 1;
+        const float r0 = __shfl_xor_sync(0xffffffffu, b2 ? part[0] : part[2], 4);
+        const float r1 = __shfl_xor_sync(0xffffffffu, b2 ? part[1] : part[3], 4);
+        const float x0 = (b2 ? part[2] : part[0]) + r0;
+        const float x1 = (b2 ? part[3] : part[1]) + r1;
+        const float r = __shfl_xor_sync(0xffffffffu, b1 ? x0 : x1, 2);
+        float y = (b1 ? x1 : x0) + r;
+        y += __shfl_xor_sync(0xffffffffu, y, 1);
+        s[j] = (t < valid) ? y : -INFINITY;
+      }
+      // ---- online softmax update for head hh ----
+      float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = exp2f(m_run - m_new);
+      float p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p[j] = exp2f(s[j] - m_new);
+      l_run = l_run * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+      m_run = m_new;
+      if ((c & 1) == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sm.pbuf[g][4 * j + t4][hh] = make_float2(p[j], p[j]);
+      }
+      float alpha_h[kGroup];
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) alpha_h[h] = __shfl_sync(0xffffffffu, alpha, 2 * h);
+      __syncwarp();
+      // ---- PV: lane owns dims (2 lane, 2 lane + 1) of the four heads ----
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) acc[h] = __fmul2_rn(acc[h], make_float2(alpha_h[h], alpha_h[h]));
+      const uint8_t *vrow = Vg + lane * 4;
+      for (int t = 0; t < valid; ++t) {
+        const uint32_t vw = *reinterpret_cast<const uint32_t *>(vrow + t * kRowBytes);
+        const float2 v = make_float2(bf16_lo(vw), bf16_hi(vw));
+        const float4 p01 = *reinterpret_cast<const float4 *>(&sm.pbuf[g][t][0]);
+        const float4 p23 = *reinterpret_cast<const float4 *>(&sm.pbuf[g][t][2]);
+        acc[0] = __ffma2_rn(make_float2(p01.x, p01.y), v, acc[0]);
+        acc[1] = __ffma2_rn(make_float2(p01.z, p01.w), v, acc[1]);
+        acc[2] = __ffma2_rn(make_float2(p23.x, p23.y), v, acc[2]);
+        acc[3] = __ffma2_rn(make_float2(p23.z, p23.w), v, acc[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[st]);
+
+    const bool seq_end = (w.lp == w.n - 1);
+    if (seq_end || i == count - 1) {
+      // ---- finish this sequence's share: direct output or a partial state ----
+      float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+      float l_h[kGroup];
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) l_h[h] = __shfl_sync(0xffffffffu, lt, 2 * h);
+      if (has_first && seq_end) {
+        float *o = a.out + ((long long)w.s * kQHeads + g * kGroup) * kHeadDim + 2 * lane;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          const float inv = l_h[h] > 0.f ? 1.f / l_h[h] : 0.f;
+          *reinterpret_cast<float2 *>(o + h * kHeadDim) = make_float2(acc[h].x * inv, acc[h].y * inv);
+        }
+      } else {
+        const long long slot = (long long)cta + w.s;
+        float *o = a.part_acc + (slot * kQHeads + g * kGroup) * kHeadDim + 2 * lane;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) *reinterpret_cast<float2 *>(o + h * kHeadDim) = acc[h];
+        const float m_mine = __shfl_sync(0xffffffffu, m_run, 2 * (lane & 3));
+        const float l_mine = __shfl_sync(0xffffffffu, lt, 2 * (lane & 3));
+        if (lane < kGroup) a.part_ml[slot * kQHeads + g * kGroup + lane] = make_float2(m_mine, l_mine);
+      }
+      if (has_first && g == 0 && lane == 0) {
+        const long long T_ = sm.total_pages;
+        a.seq_info[w.s] = make_int2(cta, cta_of_page(gfirst + w.n - 1, T_, G));
+      }
+      if (i + 1 < count) {
+        w.next(a);
+        load_q(a, w.s, g, c, qf);
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) acc[h] = make_float2(0.f, 0.f);
+        has_first = true;
+        gfirst = pa + i + 1;
+      }
+    } else {
+      w.next(a);
+    }
+  }
+}
+
+// Combines the partial states of sequences split across CTAs:
+//   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  out = sum_c acc_c 2^(m_c - M) / L.
+// Also writes the zero rows of empty or invalid sequences.
+__global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const DecodeArgs a) {
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int h = tid >> 3, d0 = (tid & 7) * 8;
+  float *o = a.out + ((long long)s * kQHeads + h) * kHeadDim + d0;
+  const int ctx = __ldg(a.context_lens + s);
+  if (ctx <= 0 || ctx > a.max_context) {
+    reinterpret_cast<float4 *>(o)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4 *>(o)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int2 info = a.seq_info[s];
+  if (info.x == info.y) return;  // written directly by its only CTA
+  // CTAs between the first and the last may own no pages at all (more CTAs than
+  // pages); they left no partial and are skipped.
+  const long long T = a.meta[0];
+  const long long G = a.meta[1];
+  float M = -INFINITY;
+  for (int c = info.x; c <= info.y; ++c) {
+    if ((long long)c * T / G == (long long)(c + 1) * T / G) continue;
+    M = fmaxf(M, a.part_ml[((long long)c + s) * kQHeads + h].x);
+  }
+  float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int c = info.x; c <= info.y; ++c) {
+      if ((long long)c * T / G == (long long)(c + 1) * T / G) continue;
+      const long long slot = (long long)c + s;
+      const float2 ml = a.part_ml[slot * kQHeads + h];
+      const float wgt = exp2f(ml.x - M);
+      L += ml.y * wgt;
+      const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (slot * kQHeads + h) * kHeadDim + d0);
+      const float4 x0 = src[0], x1 = src[1];
+      r[0] += wgt * x0.x; r[1] += wgt * x0.y; r[2] += wgt * x0.z; r[3] += wgt * x0.w;
+      r[4] += wgt * x1.x; r[5] += wgt * x1.y; r[6] += wgt * x1.z; r[7] += wgt * x1.w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  reinterpret_cast<float4 *>(o)[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
+  reinterpret_cast<float4 *>(o)[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+}
+
+
+struct WorkspaceLayout {
+  long long *meta;
+  float *part_acc;
+  float2 *part_ml;
+  int2 *seq_info;
+  size_t bytes;
+};
+
+// [meta: 16 B][partial accumulators][partial (m, l)][per-sequence CTA span]
+WorkspaceLayout layout_workspace(void *base, int num_seqs) {
+  const size_t slots = size_t(kMaxCtas) + size_t(num_seqs);
+  WorkspaceLayout L;
+  uint8_t *p = static_cast<uint8_t *>(base);
+  const size_t meta_bytes = 16;
+  const size_t acc_bytes = slots * kQHeads * kHeadDim * sizeof(float);
+  const size_t ml_bytes = slots * kQHeads * sizeof(float2);
+  L.meta = reinterpret_cast<long long *>(p);
+  L.part_acc = reinterpret_cast<float *>(p + meta_bytes);
+  L.part_ml = reinterpret_cast<float2 *>(p + meta_bytes + acc_bytes);
+  L.seq_info = reinterpret_cast<int2 *>(p + meta_bytes + acc_bytes + ml_bytes);
+  L.bytes = meta_bytes + acc_bytes + ml_bytes + size_t(num_seqs) * sizeof(int2);
+  return L;
+}
+
+int auto_ctas(int num_seqs, int max_context) {
+  const int sms = device_sm_count();
+  const long long upper = (long long)num_seqs * ((max_context + kPageTokens - 1) / kPageTokens);
+  long long g = sms > 0 ? (long long)sms * kCtasPerSm : 2 * 148;
+  const long long by_work = (upper + kMinPagesPerCta - 1) / kMinPagesPerCta;
+  if (by_work < g) g = by_work;
+  if (g < 1) g = 1;
+  if (g > kMaxCtas) g = kMaxCtas;
+  return int(g);
+}
+
+int setup_kernel_attributes() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(paged_decode_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(sizeof(Smem)));
+  });
+  return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
+           int64_t bt_stride, const int32_t *context_lens, int num_seqs, int max_context, float scale,
+           void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream) {
+  int rc = check_pool(pool);
+  if (rc != PKV_OK) return rc;
+  if (num_q_heads != kQHeads) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || max_context < 0 || bt_stride < 0 || num_ctas < 0 || num_ctas > kMaxCtas)
+    return PKV_ERR_SHAPE;
+  if (num_seqs > (1 << 24)) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr || workspace == nullptr)
+    return PKV_ERR_NULL;
+  if (!isfinite(scale)) return PKV_ERR_SCALE;
+  if (!aligned16(q) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(out) & 7u) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return PKV_ERR_ALIGN;
+  const WorkspaceLayout L = layout_workspace(workspace, num_seqs);
+  if (workspace_bytes < L.bytes) return PKV_ERR_WORKSPACE;
+  rc = setup_kernel_attributes();
+  if (rc != PKV_OK) return rc;
+
+  DecodeArgs a;
+  a.k_base = static_cast<const uint8_t *>(pool->k_base);
+  a.v_base = static_cast<const uint8_t *>(pool->v_base);
+  a.page_stride = pool->page_stride_bytes;
+  a.num_pages = pool->num_pages;
+  a.q = static_cast<const uint4 *>(q);
+  a.out = out;
+  a.block_tables = block_tables;
+  a.bt_stride = bt_stride;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.max_context = max_context;
+  a.scale_log2 = scale * kLog2e;
+  a.part_acc = L.part_acc;
+  a.part_ml = L.part_ml;
+  a.seq_info = L.seq_info;
+  a.meta = L.meta;
+  a.status = device_status;
+
+  const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  paged_decode_partial_kernel<<<G, kThreads, sizeof(Smem), st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
+  // A single CTA covers every sequence whole and writes the output itself, but
+  // sequences with no pages still need their zero rows from the merge kernel.
+  paged_decode_merge_kernel<<<num_seqs, kMergeThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim) {
+  if (num_seqs < 0 || num_q_heads != pkv::kQHeads || head_dim != pkv::kHeadDim) return 0;
+  return pkv::layout_workspace(nullptr, num_seqs).bytes;
+}
+
+extern "C" int pkv_decode_max_ctas(void) { return pkv::kMaxCtas; }
+
+extern "C" int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches) {
+  if (num_seqs < 0 || max_context < 0) return PKV_ERR_SHAPE;
+  const int g = num_seqs == 0 ? 0 : pkv::auto_ctas(num_seqs, max_context);
+  if (num_ctas) *num_ctas = g;
+  if (launches) *launches = num_seqs == 0 ? 0 : 2;
+  return PKV_OK;
+}
+
+extern "C" int pkv_paged_decode_attention(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                          const int32_t *block_tables, int64_t block_table_stride,
+                                          const int32_t *context_lens, int num_seqs, int max_context, float scale,
+                                          void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                          void *stream) {
+  return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
+                     max_context, scale, workspace, workspace_bytes, device_status, 0, stream);
+}
+
+extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                               const int32_t *block_tables, int64_t block_table_stride,
+                                               const int32_t *context_lens, int num_seqs, int max_context,
+                                               float scale, void *workspace, size_t workspace_bytes,
+                                               int32_t *device_status, int num_ctas, void *stream) {
+  return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
+                     max_context, scale, workspace, workspace_bytes, device_status, num_ctas, stream);
+}

@@ -1,0 +1,33 @@
+// Host-side helpers shared by the C-ABI translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The one geometry this build compiles.
+inline bool supported_geometry(int page_tokens, int num_kv_heads, int head_dim) {
+  return page_tokens == 16 && num_kv_heads == 8 && head_dim == 64;
+}
+
+// Checks a pool descriptor; PKV_OK or an error code.
+inline int check_pool(const pkv_pool *pool) {
+  if (pool == nullptr || pool->k_base == nullptr || pool->v_base == nullptr) return PKV_ERR_NULL;
+  if (pool->num_pages <= 0) return PKV_ERR_SHAPE;
+  if (!supported_geometry(pool->page_tokens, pool->num_kv_heads, pool->head_dim)) return PKV_ERR_UNSUPPORTED;
+  const int64_t half = int64_t(pool->num_kv_heads) * pool->page_tokens * pool->head_dim * 2;
+  if (pool->page_stride_bytes < half) return PKV_ERR_SHAPE;
+  if (!aligned16(pool->k_base) || !aligned16(pool->v_base) || (pool->page_stride_bytes & 15) != 0)
+    return PKV_ERR_ALIGN;
+  return PKV_OK;
+}
+
+// Number of SMs of the current device (cached per device); 0 if it cannot be queried.
+int device_sm_count();
+
+}  // namespace pkv

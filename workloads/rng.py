@@ -22,7 +22,10 @@ Generators used (named published methods, written from their definitions):
 """
 from __future__ import annotations
 
+import ctypes
 import os
+import subprocess
+import threading
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -33,7 +36,8 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _TWO_M53 = float(2.0 ** -53)
 
 # Work is split into chunks of this many elements and spread over host threads
-# (numpy ufuncs release the GIL), so gigabyte-sized pools generate in seconds.
+# (ctypes releases the GIL during the C calls), so gigabyte-sized pools generate
+# in seconds.
 _CHUNK = 1 << 22
 
 
@@ -91,6 +95,44 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
+_FAST_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "fastgen.c")
+_FAST_LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfastgen.so")
+_fast = None
+_fast_lock = threading.Lock()
+
+
+def build_fast(force: bool = False) -> str:
+    """Compile the C version of the generator (same definitions) next to its source."""
+    if force or not os.path.exists(_FAST_LIB) or os.path.getmtime(_FAST_LIB) < os.path.getmtime(_FAST_SRC):
+        tmp = _FAST_LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared",
+                               "-fPIC", "-o", tmp, _FAST_SRC, "-lm"])
+        os.replace(tmp, _FAST_LIB)
+    return _FAST_LIB
+
+
+def _fast_lib():
+    global _fast
+    with _fast_lock:
+        if _fast is None:
+            L = ctypes.CDLL(build_fast())
+            L.fastgen_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                              ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_void_p]
+            L.fastgen_normal_bf16.restype = None
+            _fast = L
+    return _fast
+
+
+def normal_bf16_reference(key: int, start: int, count: int, spike_key: int | None = None,
+                          spike_prob: float = 0.0, spike_factor: float = 8.0) -> np.ndarray:
+    """The numpy definition of ``normal_bf16`` (slow; the C version must match it bit for bit)."""
+    x = _normal_chunk(key, start, count)
+    if spike_key is not None and spike_prob > 0.0:
+        hit = uniform(spike_key, start, count) < spike_prob
+        x = np.where(hit, x * spike_factor, x)
+    return f64_to_bf16_bits(x)
+
+
 def normal_bf16(key: int, start: int, count: int, threads: int | None = None,
                 spike_key: int | None = None, spike_prob: float = 0.0,
                 spike_factor: float = 8.0) -> np.ndarray:
@@ -98,18 +140,17 @@ def normal_bf16(key: int, start: int, count: int, threads: int | None = None,
 
     With ``spike_key`` set, element i is multiplied by ``spike_factor`` when
     ``uniform(spike_key, i) < spike_prob`` (an independent Bernoulli per element),
-    before rounding.
+    before rounding.  Runs the C version of the definitions over host threads.
     """
     out = np.empty(count, dtype=np.uint16)
     threads = threads or min(16, os.cpu_count() or 1)
+    lib = _fast_lib()
+    use_spike = int(spike_key is not None and spike_prob > 0.0)
 
     def work(lo: int) -> None:
         n = min(_CHUNK, count - lo)
-        x = _normal_chunk(key, start + lo, n)
-        if spike_key is not None and spike_prob > 0.0:
-            hit = uniform(spike_key, start + lo, n) < spike_prob
-            x = np.where(hit, x * spike_factor, x)
-        out[lo:lo + n] = f64_to_bf16_bits(x)
+        lib.fastgen_normal_bf16(key, start + lo, n, spike_key or 0, float(spike_prob), float(spike_factor),
+                                use_spike, out[lo:].ctypes.data)
 
     starts = list(range(0, count, _CHUNK))
     if len(starts) <= 1 or threads <= 1:
