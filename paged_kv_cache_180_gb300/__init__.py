@@ -3,7 +3,20 @@
 The compute path is the C-ABI library ``libpkv.so`` (hand-written CUDA kernels,
 declared in ``include/pkv.h``); ``binding`` is its thin Python wrapper.  Build the
 library with ``python -m paged_kv_cache_180_gb300.build``.
+
+The public names below load the binding on first use; if ``libpkv.so`` is
+missing that raises ImportError (there is no fallback path).
 """
-from . import binding  # noqa: F401  (fails loudly when libpkv.so is missing)
-from .binding import (KVPool, decode_max_ctas, decode_plan, decode_workspace_bytes, kv_append,  # noqa: F401
-                      kv_pool_bytes, kv_pool_create, paged_decode_attention, status_string)
+_PUBLIC = ("KVPool", "PkvError", "PkvPool", "decode_max_ctas", "decode_plan", "decode_workspace_bytes",
+           "kv_append", "kv_pool_bytes", "kv_pool_create", "paged_decode_attention", "status_string")
+
+
+def __getattr__(name):
+    if name in _PUBLIC or name == "binding":
+        import importlib
+        binding = importlib.import_module(__name__ + ".binding")
+        return binding if name == "binding" else getattr(binding, name)
+    raise AttributeError(name)
+
+
+__all__ = list(_PUBLIC)
