@@ -62,6 +62,7 @@ extern "C" {
 #define PKV_ERR_EXCEEDS_POOL (-9)  /* scheduler: a request's page budget exceeds the whole pool */
 #define PKV_ERR_NO_PAGE (-10)      /* allocator: no free page */
 #define PKV_ERR_STATE (-11)        /* scheduler/allocator used out of order */
+#define PKV_ERR_NOALLOC_LIMIT (-12) /* num_seqs above the fixed scratch of the allocation-free entry point */
 
 /* ---- device status bits (OR-ed into *device_status) --------------------- */
 #define PKV_DEV_BAD_SLOT 1u        /* kv_append: slot >= num_pages * page_tokens; token not written */
@@ -184,6 +185,34 @@ int pkv_decode_max_ctas(void);
  * split-context pass and kernel launches per call.  Returns PKV_OK or an error.
  */
 int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches);
+
+/*
+ * pkv_paged_decode_attention_noalloc - pkv_paged_decode_attention for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers have no way to obtain a workspace: a plugin loaded into a host runtime
+ * that owns every device buffer and hands out only inputs and outputs, or a C/FFI
+ * caller with no device allocator of its own that must not call cudaMalloc (which can
+ * synchronise the device and fail under memory pressure mid-run).  This entry point
+ * takes the same inputs and output but no workspace: the split-context partial states
+ * live in one fixed array of device memory inside this library, sized for
+ * PKV_NOALLOC_MAX_SEQS sequences (about 12.4 MiB), which every GPU that loads the
+ * library holds until the process exits.  It calls no allocator.
+ *
+ *  - num_seqs > PKV_NOALLOC_MAX_SEQS returns PKV_ERR_NOALLOC_LIMIT and enqueues nothing.
+ *  - The first call on a device (with that device current) looks up the array's device
+ *    address once; make that first call before any stream capture on that device.
+ *  - All calls on a device share the one array and it keeps the last call's contents.
+ *    Nothing in it has to start at zero (every value read is written earlier in the same
+ *    call), but calls that overlap on the GPU - on different streams, or from different
+ *    host threads without ordering - race on it: serialise them.
+ * Other arguments, errors and results are those of pkv_paged_decode_attention.
+ */
+#define PKV_NOALLOC_MAX_SEQS 512
+int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                       const int32_t *block_tables, int64_t block_table_stride,
+                                       const int32_t *context_lens, int num_seqs, int max_context,
+                                       float scale, int32_t *device_status, void *stream);
 
 /* Short English text for a PKV_ERR_* code or PKV_OK. */
 const char *pkv_status_string(int status);

@@ -8,7 +8,8 @@ The public names below load the binding on first use; if ``libpkv.so`` is
 missing that raises ImportError (there is no fallback path).
 """
 _PUBLIC = ("KVPool", "PkvError", "PkvPool", "decode_max_ctas", "decode_plan", "decode_workspace_bytes",
-           "kv_append", "kv_pool_bytes", "kv_pool_create", "paged_decode_attention", "status_string")
+           "kv_append", "kv_pool_bytes", "kv_pool_create", "paged_decode_attention",
+           "paged_decode_attention_noalloc", "status_string")
 
 
 def __getattr__(name):

@@ -52,7 +52,10 @@ EXPORTS = {
     "pkv_decode_max_ctas": (_I, []),
     "pkv_decode_plan": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
+    "pkv_paged_decode_attention_noalloc": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _P]),
 }
+
+NOALLOC_MAX_SEQS = 512  # PKV_NOALLOC_MAX_SEQS
 
 for _name, (_res, _args) in EXPORTS.items():
     _fn = getattr(_lib, _name)
@@ -164,3 +167,21 @@ def paged_decode_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.T
                                              num_seqs, max_context, scale, _ptr(workspace), ws_bytes,
                                              _ptr(status), _stream(stream))
     _check("pkv_paged_decode_attention", rc)
+
+
+def paged_decode_attention_noalloc(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.Tensor,
+                                   block_tables: torch.Tensor, block_table_stride: int, context_lens: torch.Tensor,
+                                   max_context: int, scale: float, status: torch.Tensor | None = None,
+                                   stream=None) -> None:
+    """paged_decode_attention without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps the split-context partial states in one fixed device array (up to
+    NOALLOC_MAX_SEQS sequences) shared by every call on a device: calls must not overlap on the
+    GPU, and the first call on a device should come before any stream capture there.
+    """
+    desc = pool.desc if isinstance(pool, KVPool) else pool
+    num_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+    rc = _lib.pkv_paged_decode_attention_noalloc(ctypes.byref(desc), _ptr(out), _ptr(q), num_q_heads,
+                                                 _ptr(block_tables), block_table_stride, _ptr(context_lens),
+                                                 num_seqs, max_context, scale, _ptr(status), _stream(stream))
+    _check("pkv_paged_decode_attention_noalloc", rc)

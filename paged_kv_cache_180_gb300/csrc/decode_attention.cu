@@ -560,3 +560,67 @@ extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out,
   return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
                      max_context, scale, workspace, workspace_bytes, device_status, num_ctas, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  The workspace of pkv_paged_decode_attention lives in
+// a fixed device array of this file, sized for PKV_NOALLOC_MAX_SEQS sequences,
+// for callers that cannot allocate device memory.  Its device address is looked
+// up once per device (cudaGetSymbolAddress on the first call with that device
+// current); the call then follows the regular path with that address as the
+// workspace.  No value in the array needs to start at zero: every partial state,
+// span and total the merge reads is written earlier in the same call.
+namespace pkv {
+namespace {
+
+constexpr size_t kNoallocScratchBytes =
+    16 + (size_t(kMaxCtas) + PKV_NOALLOC_MAX_SEQS) * (size_t(kQHeads) * kHeadDim * sizeof(float) +
+                                                      size_t(kQHeads) * sizeof(float2)) +
+    size_t(PKV_NOALLOC_MAX_SEQS) * sizeof(int2);
+
+}  // namespace
+}  // namespace pkv
+
+static __device__ __align__(256) unsigned char pkv_noalloc_scratch[pkv::kNoallocScratchBytes];
+
+namespace pkv {
+namespace {
+
+// Device address of pkv_noalloc_scratch on the current device, or nullptr.
+void *noalloc_scratch_address() {
+  static std::mutex mu;
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, pkv_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                                  const int32_t *block_tables, int64_t block_table_stride,
+                                                  const int32_t *context_lens, int num_seqs, int max_context,
+                                                  float scale, int32_t *device_status, void *stream) {
+  if (num_seqs > PKV_NOALLOC_MAX_SEQS) return PKV_ERR_NOALLOC_LIMIT;
+  if (num_seqs <= 0) {
+    return num_seqs < 0 ? PKV_ERR_SHAPE : PKV_OK;
+  }
+  const size_t need = pkv::layout_workspace(nullptr, num_seqs).bytes;
+  if (need > pkv::kNoallocScratchBytes) return PKV_ERR_NOALLOC_LIMIT;
+  void *scratch = pkv::noalloc_scratch_address();
+  if (scratch == nullptr) return PKV_ERR_CUDA;
+  return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
+                     max_context, scale, scratch, pkv::kNoallocScratchBytes, device_status, 0, stream);
+}
