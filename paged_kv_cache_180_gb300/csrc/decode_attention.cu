@@ -22,22 +22,24 @@
 //    leaves one partial state (m, l, acc) per CTA in the workspace, combined by
 //    the merge kernel.  The partial of (CTA c, sequence s) lives in slot c + s,
 //    unique because the (c, s) pairs of the list form a monotone staircase.
-//  * Staging: one producer thread streams whole pages (16 KiB of K, 16 KiB of V,
-//    contiguous in the pool) with 1-D bulk TMA copies into a ring of shared
-//    memory stages guarded by mbarriers; eight consumer warps (one per K/V head)
-//    read each page once from shared memory and serve all four query heads of
-//    their group from that single read.
-//  * Scores: lane (t4, c) of a warp holds q[8c .. 8c+7] of the four query heads
-//    (pre-multiplied by scale*log2(e), so the softmax runs on exp2); for
-//    tokens t = 4j + t4 it dots a 16-byte K chunk with packed FP32x2 FMAs and
-//    reduces across the eight chunk lanes with a transposing butterfly that
-//    leaves each lane one (token, head) score.
-//  * Softmax: running max and sum per head with warp shuffles; probabilities of a
-//    page go through 512 B of shared memory to the PV lanes.
-//  * PV: lane owns dims (2*lane, 2*lane+1) of the four heads and accumulates
-//    p * V with packed FMAs; V rows are read as 128 contiguous bytes per warp.
+//  * Staging: one producer thread streams each page as two tiled TMA boxes (the
+//    K half and the V half: 8 heads x 16 tokens x 128 B rows) into a ring of
+//    shared-memory stages guarded by mbarriers.  The boxes land 128-byte
+//    swizzled (16-byte chunk c of row r stored at chunk c ^ (r % 8)), so the
+//    ldmatrix reads below are free of bank conflicts.
+//  * Math on the tensor cores, one warp per K/V head serving its 4 query heads:
+//    S[16 x 16] = Q[16 x 64] K^T (rows 0-3 are the group's query heads, rows
+//    4-15 zero) as 2 x 4 mma.sync m16n8k16 (bf16 in, fp32 accumulate), K read
+//    with ldmatrix; the online softmax (exp2, scale*log2(e) applied to the fp32
+//    scores) runs on the accumulator fragments with quad shuffles; the
+//    probabilities stay in registers as the A operand of O[16 x 64] += P V
+//    (8 n-tiles, V read with ldmatrix.trans).  P is split into bf16 hi + lo
+//    parts (two MMAs each) so the weights keep ~16 significant bits.  Tokens
+//    past the context in a sequence's last page get score -inf and their V
+//    fragments are zeroed, so stale pool bytes (even NaN) never reach the sums.
 //  * Every mbarrier wait is bounded (about 2 s); on expiry the CTA reports
 //    PKV_DEV_TIMEOUT and stops, after draining its outstanding copies.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -56,15 +58,15 @@ constexpr int kMaxCtas = 1024;
 constexpr int kCtasPerSm = 2;
 constexpr int kMinPagesPerCta = 2;
 constexpr int kMergeThreads = 256;
+constexpr int kBoxRows = kKvHeads * kPageTokens;  // 128 rows of 128 B per K (or V) half page
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
-  const uint8_t *k_base;
-  const uint8_t *v_base;
-  long long page_stride;
+  CUtensorMap tmap_k;  // K halves: dims (64 elems, 128 rows, pages), 128B swizzle
+  CUtensorMap tmap_v;  // V halves, same shape
   int num_pages;
-  const uint4 *q;  // [num_seqs][32][64] bf16, 8 uint4 per head
-  float *out;      // [num_seqs][32][64]
+  const uint32_t *q;  // [num_seqs][32][64] bf16, as 32 packed pairs per head
+  float *out;         // [num_seqs][32][64]
   const int32_t *block_tables;
   long long bt_stride;
   const int32_t *context_lens;
@@ -78,9 +80,8 @@ struct DecodeArgs {
   int32_t *status;
 };
 
-struct __align__(128) Smem {
-  uint8_t kv[kStages][2][kHalfPageBytes];
-  float2 pbuf[kConsumerWarps][kPageTokens][kGroup];  // (p, p) pairs per (token, head)
+struct __align__(1024) Smem {
+  uint8_t kv[kStages][2][kHalfPageBytes];  // each half 1024-byte aligned (swizzle atom)
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int stage_ok[kStages];
@@ -90,6 +91,7 @@ struct __align__(128) Smem {
   int seq0;
   int found;
 };
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the dynamic base to 1024 B
 
 __device__ __forceinline__ int seq_pages(int ctx, int max_context) {
   return (ctx > 0 && ctx <= max_context) ? (ctx + kPageTokens - 1) / kPageTokens : 0;
@@ -136,22 +138,26 @@ struct Walk {
   }
 };
 
-__device__ __forceinline__ void load_q(const DecodeArgs &a, int s, int g, int c, float (&qf)[kGroup][8]) {
+// A-operand fragments of Q for the four k-steps: lane < 16 holds query head
+// 4g + lane/4, dims 16ks + 2(lane%4) (+1) and 16ks + 8 + 2(lane%4) (+1); lanes
+// 16..31 are the zero rows 4..7.
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int s, int g, int lane, uint32_t (&qa)[4][2]) {
+  if (lane < 16) {
+    const uint32_t *row = a.q + ((long long)s * kQHeads + g * kGroup + (lane >> 2)) * (kHeadDim / 2);
 #pragma unroll
-  for (int h = 0; h < kGroup; ++h) {
-    const uint4 w = __ldg(a.q + ((long long)s * kQHeads + g * kGroup + h) * 8 + c);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      qf[h][2 * i] = bf16_lo(ws[i]) * a.scale_log2;
-      qf[h][2 * i + 1] = bf16_hi(ws[i]) * a.scale_log2;
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks][0] = __ldg(row + ks * 8 + (lane & 3));
+      qa[ks][1] = __ldg(row + ks * 8 + 4 + (lane & 3));
     }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) qa[ks][0] = qa[ks][1] = 0u;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -216,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   if (warp == kConsumerWarps) {
     // ================= producer: one thread streams pages =================
     if (lane != 0) return;
+    prefetch_tensormap(&a.tmap_k);
+    prefetch_tensormap(&a.tmap_v);
     const uint64_t policy = policy_evict_first();
     long long issued = 0;
     bool ok = true;
@@ -231,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       if (page >= 0 && page < a.num_pages) {
         sm.stage_ok[st] = 1;
         mbar_arrive_expect_tx(&sm.full[st], 2 * kHalfPageBytes);
-        bulk_load(sm.kv[st][0], a.k_base + (long long)page * a.page_stride, kHalfPageBytes, &sm.full[st], policy);
-        bulk_load(sm.kv[st][1], a.v_base + (long long)page * a.page_stride, kHalfPageBytes, &sm.full[st], policy);
+        tma_load_3d(sm.kv[st][0], &a.tmap_k, 0, 0, page, &sm.full[st], policy);
+        tma_load_3d(sm.kv[st][1], &a.tmap_v, 0, 0, page, &sm.full[st], policy);
       } else {
         report(a.status, PKV_DEV_BAD_PAGE);
         sm.stage_ok[st] = 0;
@@ -253,14 +261,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
 
   // ================= consumers: warp g serves K/V head g =================
   const int g = warp;
-  const int t4 = lane >> 3, c = lane & 7;
-  const int hh = c >> 1;  // head (within the group) whose score this lane ends up holding
-  float qf[kGroup][8];
-  load_q(a, w.s, g, c, qf);
+  const int quad = lane & 3;     // column pair of the accumulator fragments
+  const int hrow = lane >> 2;    // fragment row: query head hrow of the group when < 4
+  // ldmatrix row addresses (byte offsets inside a stage half), fixed per lane:
+  // lane i addresses row i % 8 of matrix i / 8.
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t krow = uint32_t((g * kPageTokens + ((mi >> 1) << 3) + ri) * kRowBytes);  // K: token (mi/2)*8 + ri
+  const uint32_t kchunk = uint32_t(mi & 1);                                                 // + 2 ks
+  const uint32_t vrow = uint32_t((g * kPageTokens + ((mi & 1) << 3) + ri) * kRowBytes);   // V: token (mi%2)*8 + ri
+  const uint32_t vchunk = uint32_t(mi >> 1);                                                // + nd
+  uint32_t qa[4][2];
+  load_q(a, w.s, g, lane, qa);
   float m_run = -INFINITY, l_run = 0.f;
-  float2 acc[kGroup];
+  float o[8][4];
 #pragma unroll
-  for (int h = 0; h < kGroup; ++h) acc[h] = make_float2(0.f, 0.f);
+  for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   bool has_first = (w.lp == 0);
   long long gfirst = pa - w.lp;  // global index of the first page of the current sequence
 
@@ -272,68 +287,66 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     }
     const int valid = min(kPageTokens, w.ctx - w.lp * kPageTokens);
     if (sm.stage_ok[st]) {
-      const uint8_t *Kg = sm.kv[st][0] + g * (kPageTokens * kRowBytes);
-      const uint8_t *Vg = sm.kv[st][1] + g * (kPageTokens * kRowBytes);
-      // ---- scores: lane ends with s[j] = score(token 4j+t4, head hh) in log2 units ----
-      float s[4];
+      const uint32_t kbase = smem_addr(sm.kv[st][0]);
+      const uint32_t vbase = smem_addr(sm.kv[st][1]);
+      // ---- S = Q K^T: two n-tiles of 8 tokens, four k-steps of 16 dims ----
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int t = 4 * j + t4;
-        const uint4 kw = *reinterpret_cast<const uint4 *>(Kg + t * kRowBytes + c * 16);
-        const uint32_t ws[4] = {kw.x, kw.y, kw.z, kw.w};
-        float part[kGroup];
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-          float2 d2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2)
-            d2 = __ffma2_rn(make_float2(qf[h][2 * q2], qf[h][2 * q2 + 1]),
-                            make_float2(bf16_lo(ws[q2]), bf16_hi(ws[q2])), d2);
-          part[h] = d2.x + d2.y;
-        }
-        // transposing butterfly over the 8 chunk lanes (xor 4, 2, 1)
-        const bool b2 = (c >> 2) & 1, b1 = (c >> 1) & 1;
-        const float r0 = __shfl_xor_sync(0xffffffffu, b2 ? part[0] : part[2], 4);
-        const float r1 = __shfl_xor_sync(0xffffffffu, b2 ? part[1] : part[3], 4);
-        const float x0 = (b2 ? part[2] : part[0]) + r0;
-        const float x1 = (b2 ? part[3] : part[1]) + r1;
-        const float r = __shfl_xor_sync(0xffffffffu, b1 ? x0 : x1, 2);
-        float y = (b1 ? x1 : x0) + r;
-        y += __shfl_xor_sync(0xffffffffu, y, 1);
-        s[j] = (t < valid) ? y : -INFINITY;
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t b00, b01, b10, b11;
+        ldmatrix_x4(kbase + krow + (((2 * ks + kchunk) ^ ri) << 4), b00, b01, b10, b11);
+        mma_16816(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+        mma_16816(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
       }
-      // ---- online softmax update for head hh ----
-      float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // ---- online softmax of row hrow (tokens 8nt + 2 quad + j) ----
+      float x[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          x[nt][j] = (8 * nt + 2 * quad + j < valid) ? sc[nt][j] * a.scale_log2 : -INFINITY;
+      float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run, mx);
       const float alpha = exp2f(m_run - m_new);
-      float p[4];
+      float p[2][2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) p[j] = exp2f(s[j] - m_new);
-      l_run = l_run * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) p[nt][j] = exp2f(x[nt][j] - m_new);
+      l_run = l_run * alpha + ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
       m_run = m_new;
-      if ((c & 1) == 0) {
+      // P as the A operand of P V, split into bf16 hi + lo parts.
+      const uint32_t ph0 = pack_bf16x2(p[0][0], p[0][1]);
+      const uint32_t ph1 = pack_bf16x2(p[1][0], p[1][1]);
+      const uint32_t pl0 = pack_bf16x2(p[0][0] - bf16_lo(ph0), p[0][1] - bf16_hi(ph0));
+      const uint32_t pl1 = pack_bf16x2(p[1][0] - bf16_lo(ph1), p[1][1] - bf16_hi(ph1));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sm.pbuf[g][4 * j + t4][hh] = make_float2(p[j], p[j]);
+      for (int nd = 0; nd < 8; ++nd) {
+        o[nd][0] *= alpha;
+        o[nd][1] *= alpha;
       }
-      float alpha_h[kGroup];
+      // V fragments hold tokens 2 quad (+1) and 8 + 2 quad (+1): zero those past the context.
+      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+      if (valid < kPageTokens) {
+        const int t0 = 2 * quad;
+        vmask_lo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+        vmask_hi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+      }
+      // ---- O += P V: eight n-tiles of 8 dims, one k-step of 16 tokens ----
 #pragma unroll
-      for (int h = 0; h < kGroup; ++h) alpha_h[h] = __shfl_sync(0xffffffffu, alpha, 2 * h);
-      __syncwarp();
-      // ---- PV: lane owns dims (2 lane, 2 lane + 1) of the four heads ----
-#pragma unroll
-      for (int h = 0; h < kGroup; ++h) acc[h] = __fmul2_rn(acc[h], make_float2(alpha_h[h], alpha_h[h]));
-      const uint8_t *vrow = Vg + lane * 4;
-      for (int t = 0; t < valid; ++t) {
-        const uint32_t vw = *reinterpret_cast<const uint32_t *>(vrow + t * kRowBytes);
-        const float2 v = make_float2(bf16_lo(vw), bf16_hi(vw));
-        const float4 p01 = *reinterpret_cast<const float4 *>(&sm.pbuf[g][t][0]);
-        const float4 p23 = *reinterpret_cast<const float4 *>(&sm.pbuf[g][t][2]);
-        acc[0] = __ffma2_rn(make_float2(p01.x, p01.y), v, acc[0]);
-        acc[1] = __ffma2_rn(make_float2(p01.z, p01.w), v, acc[1]);
-        acc[2] = __ffma2_rn(make_float2(p23.x, p23.y), v, acc[2]);
-        acc[3] = __ffma2_rn(make_float2(p23.z, p23.w), v, acc[3]);
+      for (int nd = 0; nd < 8; nd += 2) {
+        uint32_t v0, v1, v2, v3;
+        ldmatrix_x4_trans(vbase + vrow + (((nd + vchunk) ^ ri) << 4), v0, v1, v2, v3);
+        v0 &= vmask_lo;
+        v1 &= vmask_hi;
+        v2 &= vmask_lo;
+        v3 &= vmask_hi;
+        mma_16816(o[nd], ph0, 0u, ph1, 0u, v0, v1);
+        mma_16816(o[nd], pl0, 0u, pl1, 0u, v0, v1);
+        mma_16816(o[nd + 1], ph0, 0u, ph1, 0u, v2, v3);
+        mma_16816(o[nd + 1], pl0, 0u, pl1, 0u, v2, v3);
       }
     }
     __syncwarp();
@@ -342,26 +355,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     const bool seq_end = (w.lp == w.n - 1);
     if (seq_end || i == count - 1) {
       // ---- finish this sequence's share: direct output or a partial state ----
-      float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
-      float l_h[kGroup];
-#pragma unroll
-      for (int h = 0; h < kGroup; ++h) l_h[h] = __shfl_sync(0xffffffffu, lt, 2 * h);
+      float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
       if (has_first && seq_end) {
-        float *o = a.out + ((long long)w.s * kQHeads + g * kGroup) * kHeadDim + 2 * lane;
+        if (hrow < kGroup) {
+          float *dst = a.out + ((long long)w.s * kQHeads + g * kGroup + hrow) * kHeadDim + 2 * quad;
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-          const float inv = l_h[h] > 0.f ? 1.f / l_h[h] : 0.f;
-          *reinterpret_cast<float2 *>(o + h * kHeadDim) = make_float2(acc[h].x * inv, acc[h].y * inv);
+          for (int nd = 0; nd < 8; ++nd)
+            *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] * inv, o[nd][1] * inv);
         }
       } else {
         const long long slot = (long long)cta + w.s;
-        float *o = a.part_acc + (slot * kQHeads + g * kGroup) * kHeadDim + 2 * lane;
+        if (hrow < kGroup) {
+          float *dst = a.part_acc + (slot * kQHeads + g * kGroup + hrow) * kHeadDim + 2 * quad;
 #pragma unroll
-        for (int h = 0; h < kGroup; ++h) *reinterpret_cast<float2 *>(o + h * kHeadDim) = acc[h];
-        const float m_mine = __shfl_sync(0xffffffffu, m_run, 2 * (lane & 3));
-        const float l_mine = __shfl_sync(0xffffffffu, lt, 2 * (lane & 3));
-        if (lane < kGroup) a.part_ml[slot * kQHeads + g * kGroup + lane] = make_float2(m_mine, l_mine);
+          for (int nd = 0; nd < 8; ++nd) *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0], o[nd][1]);
+          if (quad == 0) a.part_ml[slot * kQHeads + g * kGroup + hrow] = make_float2(m_run, lt);
+        }
       }
       if (has_first && g == 0 && lane == 0) {
         const long long T_ = sm.total_pages;
@@ -369,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       }
       if (i + 1 < count) {
         w.next(a);
-        load_q(a, w.s, g, c, qf);
+        load_q(a, w.s, g, lane, qa);
         m_run = -INFINITY;
         l_run = 0.f;
 #pragma unroll
-        for (int h = 0; h < kGroup; ++h) acc[h] = make_float2(0.f, 0.f);
+        for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
         has_first = true;
         gfirst = pa + i + 1;
       }
@@ -469,9 +480,46 @@ int setup_kernel_attributes() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(paged_decode_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(sizeof(Smem)));
+                               int(kSmemBytes));
   });
   return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map of the K (or V) halves of a pool: element (d, row, page) with row =
+// kv_head * 16 + token, row stride 128 B, page stride page_stride_bytes; one box
+// is a whole half page (64 x 128 x 1), delivered 128-byte swizzled.
+int encode_half_pages(CUtensorMap *map, const void *base, long long page_stride, int num_pages) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kBoxRows), cuuint64_t(num_pages)};
+  const cuuint64_t strides[2] = {cuuint64_t(kRowBytes), cuuint64_t(page_stride)};
+  const cuuint32_t box[3] = {cuuint32_t(kHeadDim), cuuint32_t(kBoxRows), 1u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
@@ -496,11 +544,12 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   if (rc != PKV_OK) return rc;
 
   DecodeArgs a;
-  a.k_base = static_cast<const uint8_t *>(pool->k_base);
-  a.v_base = static_cast<const uint8_t *>(pool->v_base);
-  a.page_stride = pool->page_stride_bytes;
+  rc = encode_half_pages(&a.tmap_k, pool->k_base, pool->page_stride_bytes, pool->num_pages);
+  if (rc != PKV_OK) return rc;
+  rc = encode_half_pages(&a.tmap_v, pool->v_base, pool->page_stride_bytes, pool->num_pages);
+  if (rc != PKV_OK) return rc;
   a.num_pages = pool->num_pages;
-  a.q = static_cast<const uint4 *>(q);
+  a.q = static_cast<const uint32_t *>(q);
   a.out = out;
   a.block_tables = block_tables;
   a.bt_stride = bt_stride;
@@ -516,7 +565,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
 
   const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  paged_decode_partial_kernel<<<G, kThreads, sizeof(Smem), st>>>(a);
+  paged_decode_partial_kernel<<<G, kThreads, kSmemBytes, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
   // A single CTA covers every sequence whole and writes the output itself, but
   // sequences with no pages still need their zero rows from the merge kernel.
