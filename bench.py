@@ -50,6 +50,7 @@ def parse_args():
     p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny"], default="bandwidth")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    p.add_argument("--ctas", type=int, default=0, help="CTAs of the split-context pass (0 = the library's choice)")
     return p.parse_args()
 
 
@@ -280,11 +281,13 @@ def run_native(args):
 
     dec = [tuple(to_dev(a) for a in wl.decode_tokens(layer)) for layer in range(L)]
     out = torch.empty(wl.num_seqs, 32, 64, dtype=torch.float32, device=dev)
-    ws = torch.empty(pkv.decode_workspace_bytes(wl.num_seqs), dtype=torch.uint8, device=dev)
+    ws = pkv.decode_workspace(wl.num_seqs, device=dev)
     blocks = wl.max_blocks
     stride = L * blocks
     stream = torch.cuda.current_stream(dev)
     ctas, attn_launches = pkv.decode_plan(wl.num_seqs, wl.max_context)
+    if args.ctas:
+        ctas = args.ctas
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool_bytes = wl.num_pages * 32768
@@ -301,7 +304,7 @@ def run_native(args):
             if e_marks is not None:
                 e_marks[1].record(stream)
             pkv.paged_decode_attention(pool, out, q[layer], bt.view(-1)[layer * blocks:], stride, lens,
-                                       wl.max_context, wl.scale, ws, status)
+                                       wl.max_context, wl.scale, ws, status, num_ctas=args.ctas)
             if e_marks is not None:
                 e_marks[2].record(stream)
                 e_marks = e_marks[3:]
@@ -380,7 +383,7 @@ def run_native(args):
                 kn, vn, sn = d_dec[layer]
                 pkv.kv_append(pool, kn, vn, sn, status)
                 pkv.paged_decode_attention(pool, out, d_q[layer], d_bt.view(-1)[layer * blocks:], stride, d_lens,
-                                           wl.max_context, wl.scale, ws, status)
+                                           wl.max_context, wl.scale, ws, status, num_ctas=args.ctas)
                 h_out.copy_(out, non_blocking=True)
             stream.synchronize()
 

@@ -125,8 +125,12 @@ int pkv_kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, co
                   int num_tokens, int32_t *device_status, void *stream);
 
 /*
- * Workspace bytes pkv_paged_decode_attention needs for num_seqs sequences (holds
- * split-context partial softmax states; no need to clear it).  0 on bad arguments.
+ * Workspace bytes pkv_paged_decode_attention needs for num_seqs sequences: one slot
+ * per (CTA, sequence) pair of the split, holding a partial softmax state and a
+ * ticket counter.  Zero-fill the workspace once before its first use (e.g.
+ * cudaMemsetAsync); every completed call leaves the counters at zero again, so the
+ * same workspace serves later calls of any batch size up to the one it was sized
+ * for.  After a call that reported PKV_DEV_TIMEOUT, zero it again.  0 on bad arguments.
  */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
 
@@ -150,10 +154,12 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
  *   max_context        host bound on every context_lens[s] (chooses the work split; a larger
  *                      length sets PKV_DEV_BAD_CONTEXT and zeroes that row).
  *   scale              softmax scale (1/sqrt(head_dim) for the pages' model).
- *   workspace          device, >= pkv_decode_workspace_bytes(num_seqs, ...), 16-byte aligned.
+ *   workspace          device, >= pkv_decode_workspace_bytes(num_seqs, ...), 16-byte aligned,
+ *                      zero-filled before its first use (see pkv_decode_workspace_bytes).
  *   device_status      device int32, nullable.
- * Enqueues one kernel, or two (a split-context pass and a merge) when the work is
- * split across CTAs.  Calls sharing a workspace must not overlap on the GPU.
+ * Enqueues one kernel: the pages of all sequences are split evenly over its CTAs,
+ * and the last CTA to finish a sequence that was cut merges its partial states.
+ * Calls sharing a workspace must not overlap on the GPU.
  * Returns PKV_OK or a negative PKV_ERR_* code (then nothing was enqueued).
  * Cited: samir-vllm README "What works so far" (direct paged decode attention, FP32
  * online softmax, no contiguous gather, no stored scores; separate page maps and
@@ -202,10 +208,11 @@ int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches)
  *  - num_seqs > PKV_NOALLOC_MAX_SEQS returns PKV_ERR_NOALLOC_LIMIT and enqueues nothing.
  *  - The first call on a device (with that device current) looks up the array's device
  *    address once; make that first call before any stream capture on that device.
- *  - All calls on a device share the one array and it keeps the last call's contents.
- *    Nothing in it has to start at zero (every value read is written earlier in the same
- *    call), but calls that overlap on the GPU - on different streams, or from different
- *    host threads without ordering - race on it: serialise them.
+ *  - The first call on a device also clears the array once (its merge counters must
+ *    start at zero; every completed call leaves them at zero again).
+ *  - All calls on a device share the one array and it keeps the last call's contents;
+ *    calls that overlap on the GPU - on different streams, or from different host
+ *    threads without ordering - race on it: serialise them.
  * Other arguments, errors and results are those of pkv_paged_decode_attention.
  */
 #define PKV_NOALLOC_MAX_SEQS 512

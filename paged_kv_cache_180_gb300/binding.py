@@ -138,6 +138,11 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int = 32, head_dim: int =
     return int(_lib.pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim))
 
 
+def decode_workspace(num_seqs: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for pkv_paged_decode_attention (zeroed once; calls keep it valid)."""
+    return torch.zeros(decode_workspace_bytes(num_seqs), dtype=torch.uint8, device=device)
+
+
 def decode_max_ctas() -> int:
     return int(_lib.pkv_decode_max_ctas())
 

@@ -15,16 +15,27 @@
 //
 // GB300 design
 //  * Work split: the pages of all sequences form one list (sequence-major); the
-//    grid has G CTAs (a multiple of the SM count) and CTA c takes pages
-//    [c*T/G, (c+1)*T/G) of the T pages in the list, so every CTA streams the
-//    same number of bytes whatever the mix of context lengths.  A sequence
+//    grid has G CTAs (2 per SM) and, from the lengths it reads on the device,
+//    the kernel picks how many of them (Gu) share the T pages: CTA c takes pages
+//    [c*T/Gu, (c+1)*T/Gu), so every CTA streams the same number of bytes
+//    whatever the mix of context lengths.  Equal-length batches are split along
+//    sequence boundaries instead (a cut costs a merge), and no CTA gets fewer
+//    than 8 pages unless the caller fixes the count.  A sequence
 //    covered by one CTA is written out directly; a sequence cut across CTAs
-//    leaves one partial state (m, l, acc) per CTA in the workspace, combined by
-//    the merge kernel.  The partial of (CTA c, sequence s) lives in slot c + s,
-//    unique because the (c, s) pairs of the list form a monotone staircase.
-//  * Staging: one producer thread streams each page as two tiled TMA boxes (the
-//    K half and the V half: 8 heads x 16 tokens x 128 B rows) into a ring of
-//    shared-memory stages guarded by mbarriers.  The boxes land 128-byte
+//    leaves one partial state (m, l, acc) per CTA in the workspace, and the
+//    last of those CTAs to finish (an atomic ticket on a counter, no waiting)
+//    merges them with the rule above: one launch per call.  The partial of
+//    (CTA c, sequence s) lives in slot c + s, unique because the (c, s) pairs
+//    of the list form a monotone staircase; the ticket counter of s lives in
+//    slot (first CTA of s) + s and is reset by the merging CTA, so a zeroed
+//    workspace stays valid across calls of any batch size.  Sequences with no
+//    pages (context 0 or invalid) get zero rows from CTA s % G.
+//  * Staging: each page arrives as two tiled TMA boxes (its K half and its V
+//    half: 8 heads x 16 tokens x 128 B rows, 16 KiB each, contiguous in the
+//    pool) into a ring of kStages shared-memory stages, each with an mbarrier.
+//    There is no producer warp: the CTA has one warp per K/V head, and the last
+//    warp to finish with a stage (a per-stage counter in shared memory; nobody
+//    waits) refills it with the page kStages ahead.  The boxes land 128-byte
 //    swizzled (16-byte chunk c of row r stored at chunk c ^ (r % 8)), so the
 //    ldmatrix reads below are free of bank conflicts.
 //  * Math on the tensor cores, one warp per K/V head serving its 4 query heads:
@@ -34,11 +45,15 @@
 //    scores) runs on the accumulator fragments with quad shuffles; the
 //    probabilities stay in registers as the A operand of O[16 x 64] += P V
 //    (8 n-tiles, V read with ldmatrix.trans).  P is split into bf16 hi + lo
-//    parts (two MMAs each) so the weights keep ~16 significant bits.  Tokens
+//    parts so the weights keep ~16 significant bits: the hi part fills A rows
+//    0-7 and the lo part rows 8-15, so one MMA per n-tile yields both products
+//    (accumulator halves c0/c1 and c2/c3, summed when the sequence ends).  Tokens
 //    past the context in a sequence's last page get score -inf and their V
 //    fragments are zeroed, so stale pool bytes (even NaN) never reach the sums.
-//  * Every mbarrier wait is bounded (about 2 s); on expiry the CTA reports
-//    PKV_DEV_TIMEOUT and stops, after draining its outstanding copies.
+//  * Every mbarrier wait is bounded (about 2 s); on expiry the warp reports
+//    PKV_DEV_TIMEOUT, stops waiting, computing and refilling, and walks on to the
+//    end so that all warps still meet at the same named barriers; then warp 0
+//    waits, again bounded, for any copy still in flight.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,18 +66,26 @@
 namespace pkv {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kConsumerWarps = kKvHeads;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;                // pages in flight per warp
+constexpr int kWarps = kKvHeads;          // one warp per K/V head
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kCtasPerSm = 2;
-constexpr int kMinPagesPerCta = 2;
-constexpr int kMergeThreads = 256;
-constexpr int kBoxRows = kKvHeads * kPageTokens;  // 128 rows of 128 B per K (or V) half page
+constexpr int kMinPagesPerCta = 8;  // least pages a CTA is given (unless the caller fixes the split)
+constexpr int kHeadRowsBytes = kPageTokens * kRowBytes;  // one head's K (or V) rows of a page: 2 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
+// One workspace slot: the partial state of one (CTA, sequence) pair, plus the
+// ticket counter used when this slot is a sequence's first.
+struct Slot {
+  float acc[kQHeads][kHeadDim];  // un-normalised sum of p * V
+  float2 ml[kQHeads];            // (running max in log2 units, sum of p)
+  int counter;                   // CTAs of the sequence done so far; 0 between calls
+  int pad[3];
+};
+
 struct DecodeArgs {
-  CUtensorMap tmap_k;  // K halves: dims (64 elems, 128 rows, pages), 128B swizzle
+  CUtensorMap tmap_k;  // K halves: dims (64 elems, 128 rows = head*16 + token, pages), 128B swizzle
   CUtensorMap tmap_v;  // V halves, same shape
   int num_pages;
   const uint32_t *q;  // [num_seqs][32][64] bf16, as 32 packed pairs per head
@@ -73,23 +96,26 @@ struct DecodeArgs {
   int num_seqs;
   int max_context;
   float scale_log2;  // scale * log2(e)
-  float *part_acc;   // [kMaxCtas + num_seqs][32][64]
-  float2 *part_ml;   // [kMaxCtas + num_seqs][32]  (running max in log2 units, sum)
-  int2 *seq_info;    // [num_seqs]  (first CTA, last CTA) touching the sequence
-  long long *meta;   // [2]: total pages T and CTA count G of the last split pass
+  Slot *slots;       // [kMaxCtas + num_seqs] partial states and ticket counters
   int32_t *status;
+  int exact_ctas;    // 1: split over exactly min(gridDim.x, T) CTAs (the caller chose the count)
 };
 
 struct __align__(1024) Smem {
-  uint8_t kv[kStages][2][kHalfPageBytes];  // each half 1024-byte aligned (swizzle atom)
+  uint8_t kv[kStages][2][kHalfPageBytes];  // [stage][K|V] boxes of [head][token][128 B], 1024-byte aligned
   uint64_t full[kStages];
-  uint64_t empty[kStages];
   int stage_ok[kStages];
+  unsigned stage_done[kStages];  // warps done with the stage, counted over all rounds
+  unsigned long long issued;     // pages issued so far (for the drain after a timeout)
+  int any_aborted;
   long long warp_sums[32];
+  int warp_n[32], warp_pmin[32], warp_pmax[32];
   long long total_pages;
+  int used_ctas;         // CTAs the pages are split over (<= gridDim.x)
   long long seq0_first;  // global index of the first page of seq0
   int seq0;
   int found;
+  int merge_here;        // set when this CTA is the last to finish a cut sequence
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the dynamic base to 1024 B
 
@@ -155,6 +181,54 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int s, int g, int la
   }
 }
 
+// How many of the G launched CTAs share the T pages of n sequences (pmin .. pmax
+// pages each).  Every choice is at most min(G, T), so no CTA is left without a page.
+//  * exact: the caller fixed the count.
+//  * equal-length batches: split along sequence boundaries, so that no CTA holds
+//    the end of one sequence and the start of the next: k CTAs per sequence
+//    when n <= G (k >= 1, at least kMinPagesPerCta pages each), else the largest
+//    divisor of n not above G (whole sequences per CTA) when that keeps at least
+//    half of the CTAs busy.
+//  * otherwise an even split with at least kMinPagesPerCta pages per CTA.
+__device__ int effective_ctas(int G, long long T, int n, int pmin, int pmax, int exact) {
+  if (T <= 0) return 1;
+  const long long cap = T < G ? T : G;
+  if (exact) return int(cap);
+  if (n > 0 && pmin == pmax) {
+    if (n <= G) {
+      int k = G / n;
+      const int by_pages = pmin / kMinPagesPerCta;
+      if (k > by_pages) k = by_pages;
+      if (k < 1) k = 1;
+      return n * k;
+    }
+    const int k0 = (n + G - 1) / G;
+    if (k0 <= 64) {
+      for (int k = k0; k <= 2 * k0; ++k)
+        if (n % k == 0 && n / k >= G / 2) return n / k;
+    }
+  }
+  long long g = (T + kMinPagesPerCta - 1) / kMinPagesPerCta;
+  if (g > cap) g = cap;
+  return int(g < 1 ? 1 : g);
+}
+
+// Start the copy of the page the walk points at into stage st (or mark the stage
+// empty when the page id is invalid).  One thread calls this.
+__device__ __forceinline__ void issue_page(const DecodeArgs &a, Smem &sm, int st, const Walk &w, uint64_t policy) {
+  const int page = __ldg(a.block_tables + (long long)w.s * a.bt_stride + w.lp);
+  if (page >= 0 && page < a.num_pages) {
+    sm.stage_ok[st] = 1;
+    mbar_arrive_expect_tx(&sm.full[st], 2 * kHalfPageBytes);
+    tma_load_3d(sm.kv[st][0], &a.tmap_k, 0, 0, page, &sm.full[st], policy);
+    tma_load_3d(sm.kv[st][1], &a.tmap_v, 0, 0, page, &sm.full[st], policy);
+  } else {
+    report(a.status, PKV_DEV_BAD_PAGE);
+    sm.stage_ok[st] = 0;
+    mbar_arrive(&sm.full[st]);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
@@ -164,36 +238,69 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kConsumerWarps);
+      sm.stage_done[i] = 0;
     }
     sm.found = 0;
+    sm.merge_here = 0;
+    sm.issued = 0;
+    sm.any_aborted = 0;
     mbar_init_fence();
   }
 
   // ---- total pages T, and this CTA's range [pa, pb) ----
+  // Per thread: pages, sequences with pages, and the least and most pages of one sequence.
   long long mine = 0;
+  int n_mine = 0, pmin = 0x7fffffff, pmax = 0;
   for (int i = tid; i < a.num_seqs; i += kThreads) {
     const int c = __ldg(a.context_lens + i);
-    mine += seq_pages(c, a.max_context);
+    const int p = seq_pages(c, a.max_context);
+    mine += p;
+    if (p > 0) {
+      ++n_mine;
+      pmin = min(pmin, p);
+      pmax = max(pmax, p);
+    }
     if (cta == 0 && (c < 0 || c > a.max_context)) report(a.status, PKV_DEV_BAD_CONTEXT);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if (lane == 0) sm.warp_sums[warp] = mine;
+  for (int o = 16; o > 0; o >>= 1) {
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    n_mine += __shfl_xor_sync(0xffffffffu, n_mine, o);
+    pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+    pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+  }
+  if (lane == 0) {
+    sm.warp_sums[warp] = mine;
+    sm.warp_n[warp] = n_mine;
+    sm.warp_pmin[warp] = pmin;
+    sm.warp_pmax[warp] = pmax;
+  }
   __syncthreads();
   if (tid == 0) {
     long long t = 0;
-    for (int w = 0; w < kThreads / 32; ++w) t += sm.warp_sums[w];
-    sm.total_pages = t;
-    if (cta == 0) {
-      a.meta[0] = t;
-      a.meta[1] = G;
+    int n = 0, lo = 0x7fffffff, hi = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      t += sm.warp_sums[w];
+      n += sm.warp_n[w];
+      lo = min(lo, sm.warp_pmin[w]);
+      hi = max(hi, sm.warp_pmax[w]);
     }
+    sm.total_pages = t;
+    sm.used_ctas = effective_ctas(G, t, n, lo, hi, a.exact_ctas);
   }
   __syncthreads();
   const long long T = sm.total_pages;
-  const long long pa = (long long)cta * T / G, pb = (long long)(cta + 1) * T / G;
-  if (pa >= pb) return;  // nothing assigned (uniform across the CTA)
+  // zero rows of the sequences that have no pages, spread over all launched CTAs
+  for (int s = cta; s < a.num_seqs; s += G) {
+    if (seq_pages(__ldg(a.context_lens + s), a.max_context) == 0) {
+      float4 *row = reinterpret_cast<float4 *>(a.out + (long long)s * kQHeads * kHeadDim);
+      for (int k = tid; k < kQHeads * kHeadDim / 4; k += kThreads) row[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  // The pages are split over Gu <= min(G, T) CTAs, so every CTA below Gu owns at least one page.
+  const int Gu = sm.used_ctas;
+  if (cta >= Gu) return;
+  const long long pa = (long long)cta * T / Gu, pb = (long long)(cta + 1) * T / Gu;
 
   // ---- first sequence of the range ----
   long long running = 0;
@@ -213,63 +320,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   }
   const long long count = pb - pa;
 
-  Walk w;
+  // ================= warp g: K/V head g, query heads 4g .. 4g+3 =================
+  const int g = warp;
+  Walk w;  // page being computed
   w.s = sm.seq0;
   w.ctx = __ldg(a.context_lens + w.s);
   w.n = seq_pages(w.ctx, a.max_context);
   w.lp = int(pa - sm.seq0_first);
-
-  if (warp == kConsumerWarps) {
-    // ================= producer: one thread streams pages =================
-    if (lane != 0) return;
+  Walk wi = w;  // page to issue next (kStages ahead of w once the ring is full)
+  const uint64_t policy = policy_evict_first();
+  const long long first_fill = count < kStages ? count : kStages;
+  if (tid == 0) {
     prefetch_tensormap(&a.tmap_k);
     prefetch_tensormap(&a.tmap_v);
-    const uint64_t policy = policy_evict_first();
-    long long issued = 0;
-    bool ok = true;
-    for (long long i = 0; i < count; ++i) {
-      const int st = int(i % kStages);
-      const uint32_t round = uint32_t(i / kStages);
-      if (i >= kStages && !mbar_wait(&sm.empty[st], (round - 1) & 1)) {
-        report(a.status, PKV_DEV_TIMEOUT);
-        ok = false;
-        break;
-      }
-      const int page = __ldg(a.block_tables + (long long)w.s * a.bt_stride + w.lp);
-      if (page >= 0 && page < a.num_pages) {
-        sm.stage_ok[st] = 1;
-        mbar_arrive_expect_tx(&sm.full[st], 2 * kHalfPageBytes);
-        tma_load_3d(sm.kv[st][0], &a.tmap_k, 0, 0, page, &sm.full[st], policy);
-        tma_load_3d(sm.kv[st][1], &a.tmap_v, 0, 0, page, &sm.full[st], policy);
-      } else {
-        report(a.status, PKV_DEV_BAD_PAGE);
-        sm.stage_ok[st] = 0;
-        mbar_arrive(&sm.full[st]);
-      }
-      ++issued;
-      if (i + 1 < count) w.next(a);
-    }
-    if (!ok) {
-      // Drain: wait (bounded) for the copies still landing in the stages that
-      // were issued but possibly not consumed, so none outlives the CTA.
-      const long long first = issued > kStages ? issued - kStages : 0;
-      for (long long i = first; i < issued; ++i)
-        mbar_wait(&sm.full[int(i % kStages)], uint32_t(i / kStages) & 1);
-    }
-    return;
   }
+  for (long long j = 0; j < first_fill; ++j) {
+    if (tid == 0) issue_page(a, sm, int(j), wi, policy);
+    if (j + 1 < count) wi.next(a);
+  }
+  if (tid == 0) atomicMax(&sm.issued, (unsigned long long)first_fill);
 
-  // ================= consumers: warp g serves K/V head g =================
-  const int g = warp;
   const int quad = lane & 3;     // column pair of the accumulator fragments
   const int hrow = lane >> 2;    // fragment row: query head hrow of the group when < 4
-  // ldmatrix row addresses (byte offsets inside a stage half), fixed per lane:
-  // lane i addresses row i % 8 of matrix i / 8.
+  // ldmatrix row addresses inside a 2 KiB box (lane i addresses row i % 8 of matrix i / 8)
   const int mi = lane >> 3, ri = lane & 7;
-  const uint32_t krow = uint32_t((g * kPageTokens + ((mi >> 1) << 3) + ri) * kRowBytes);  // K: token (mi/2)*8 + ri
-  const uint32_t kchunk = uint32_t(mi & 1);                                                 // + 2 ks
-  const uint32_t vrow = uint32_t((g * kPageTokens + ((mi & 1) << 3) + ri) * kRowBytes);   // V: token (mi%2)*8 + ri
-  const uint32_t vchunk = uint32_t(mi >> 1);                                                // + nd
+  const uint32_t krow = uint32_t((((mi >> 1) << 3) + ri) * kRowBytes);  // K: token (mi/2)*8 + ri
+  const uint32_t kchunk = uint32_t(mi & 1);                             // + 2 ks
+  const uint32_t vrow = uint32_t((((mi & 1) << 3) + ri) * kRowBytes);   // V: token (mi%2)*8 + ri
+  const uint32_t vchunk = uint32_t(mi >> 1);                            // + nd
   uint32_t qa[4][2];
   load_q(a, w.s, g, lane, qa);
   float m_run = -INFINITY, l_run = 0.f;
@@ -278,17 +356,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   bool has_first = (w.lp == 0);
   long long gfirst = pa - w.lp;  // global index of the first page of the current sequence
+  bool aborted = false;          // a wait gave up: stop waiting, computing and issuing, keep walking
 
   for (long long i = 0; i < count; ++i) {
     const int st = int(i % kStages);
-    if (!mbar_wait(&sm.full[st], uint32_t(i / kStages) & 1)) {
+    if (!aborted && !mbar_wait(&sm.full[st], uint32_t(i / kStages) & 1)) {
       report(a.status, PKV_DEV_TIMEOUT);
-      return;
+      aborted = true;
     }
     const int valid = min(kPageTokens, w.ctx - w.lp * kPageTokens);
-    if (sm.stage_ok[st]) {
-      const uint32_t kbase = smem_addr(sm.kv[st][0]);
-      const uint32_t vbase = smem_addr(sm.kv[st][1]);
+    if (!aborted && sm.stage_ok[st]) {
+      const uint32_t kbase = smem_addr(sm.kv[st][0]) + g * kHeadRowsBytes;
+      const uint32_t vbase = smem_addr(sm.kv[st][1]) + g * kHeadRowsBytes;
       // ---- S = Q K^T: two n-tiles of 8 tokens, four k-steps of 16 dims ----
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -326,6 +405,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       for (int nd = 0; nd < 8; ++nd) {
         o[nd][0] *= alpha;
         o[nd][1] *= alpha;
+        o[nd][2] *= alpha;
+        o[nd][3] *= alpha;
       }
       // V fragments hold tokens 2 quad (+1) and 8 + 2 quad (+1): zero those past the context.
       uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
@@ -343,18 +424,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
         v1 &= vmask_hi;
         v2 &= vmask_lo;
         v3 &= vmask_hi;
-        mma_16816(o[nd], ph0, 0u, ph1, 0u, v0, v1);
-        mma_16816(o[nd], pl0, 0u, pl1, 0u, v0, v1);
-        mma_16816(o[nd + 1], ph0, 0u, ph1, 0u, v2, v3);
-        mma_16816(o[nd + 1], pl0, 0u, pl1, 0u, v2, v3);
+        // A rows 0-7 carry P_hi and rows 8-15 P_lo: c0/c1 gather P_hi V, c2/c3 P_lo V.
+        mma_16816(o[nd], ph0, pl0, ph1, pl1, v0, v1);
+        mma_16816(o[nd + 1], ph0, pl0, ph1, pl1, v2, v3);
       }
     }
+    // ---- the last warp done with this stage refills it with the page kStages ahead ----
+    // Every ldmatrix result of this stage has been consumed by an instruction above,
+    // so the warp's reads are complete once all lanes reach this point.
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[st]);
+    if (i + kStages < count) {
+      if (lane == 0 && !aborted) {
+        const unsigned done = atomicAdd(&sm.stage_done[st], 1u) + 1u;
+        if (done % kWarps == 0) {
+          issue_page(a, sm, st, wi, policy);
+          atomicMax(&sm.issued, (unsigned long long)(i + kStages + 1));
+        }
+      }
+      wi.next(a);
+    }
+    if (aborted && lane == 0) sm.any_aborted = 1;
 
     const bool seq_end = (w.lp == w.n - 1);
     if (seq_end || i == count - 1) {
-      // ---- finish this sequence's share: direct output or a partial state ----
+      // ---- finish this sequence's share: direct output, or a partial state and maybe the merge ----
       float lt = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
       lt += __shfl_xor_sync(0xffffffffu, lt, 2);
       if (has_first && seq_end) {
@@ -363,20 +456,62 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
           const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
           for (int nd = 0; nd < 8; ++nd)
-            *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] * inv, o[nd][1] * inv);
+            *reinterpret_cast<float2 *>(dst + 8 * nd) =
+                make_float2((o[nd][0] + o[nd][2]) * inv, (o[nd][1] + o[nd][3]) * inv);
         }
       } else {
-        const long long slot = (long long)cta + w.s;
+        Slot &mine = a.slots[(long long)cta + w.s];
         if (hrow < kGroup) {
-          float *dst = a.part_acc + (slot * kQHeads + g * kGroup + hrow) * kHeadDim + 2 * quad;
+          float *dst = &mine.acc[g * kGroup + hrow][2 * quad];
 #pragma unroll
-          for (int nd = 0; nd < 8; ++nd) *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0], o[nd][1]);
-          if (quad == 0) a.part_ml[slot * kQHeads + g * kGroup + hrow] = make_float2(m_run, lt);
+          for (int nd = 0; nd < 8; ++nd)
+            *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
+          if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
         }
-      }
-      if (has_first && g == 0 && lane == 0) {
-        const long long T_ = sm.total_pages;
-        a.seq_info[w.s] = make_int2(cta, cta_of_page(gfirst + w.n - 1, T_, G));
+        // The barrier orders every warp's partial stores before thread 0's device-scope
+        // fence and ticket (release); thread 0 fences again after the ticket (acquire)
+        // before the barrier that lets the warps read the other CTAs' partials.
+        named_barrier_sync(1, kThreads);
+        // CTAs holding pages of this sequence: c_first .. c_last, less any with an empty range.
+        const int c_first = cta_of_page(gfirst, T, Gu);
+        const int c_last = cta_of_page(gfirst + w.n - 1, T, Gu);
+        if (tid == 0) {
+          const int parts = c_last - c_first + 1;  // every CTA in the span owns pages of it
+          int *counter = &a.slots[(long long)c_first + w.s].counter;
+          __threadfence();
+          const int ticket = atomicAdd(counter, 1);
+          const int last = (ticket == parts - 1);
+          if (last) atomicExch(counter, 0);  // ready for the next call
+          __threadfence();
+          sm.merge_here = last;
+        }
+        named_barrier_sync(1, kThreads);
+        if (sm.merge_here) {
+          // warp g merges query heads 4g .. 4g+3: lane -> head 4g + lane/8, dims 8 (lane%8) .. +7
+          const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
+          float M = -INFINITY;
+#pragma unroll 8
+          for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, __ldcg(&a.slots[(long long)c + w.s].ml[h]).x);
+          float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float L = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll 4
+            for (int c = c_first; c <= c_last; ++c) {
+              const Slot &part = a.slots[(long long)c + w.s];
+              const float2 ml = __ldcg(&part.ml[h]);
+              const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
+              const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+              const float wgt = exp2f(ml.x - M);
+              L += ml.y * wgt;
+              r[0] += wgt * x0.x; r[1] += wgt * x0.y; r[2] += wgt * x0.z; r[3] += wgt * x0.w;
+              r[4] += wgt * x1.x; r[5] += wgt * x1.y; r[6] += wgt * x1.z; r[7] += wgt * x1.w;
+            }
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          float4 *dst = reinterpret_cast<float4 *>(a.out + ((long long)w.s * kQHeads + h) * kHeadDim + d0);
+          dst[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
+          dst[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+        }
       }
       if (i + 1 < count) {
         w.next(a);
@@ -392,77 +527,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       w.next(a);
     }
   }
+  named_barrier_sync(1, kThreads);
+  if (tid == 0 && sm.any_aborted) {
+    // Copies issued for pages nobody consumed: wait (bounded) so none lands after exit.
+    const long long issued = (long long)sm.issued;
+    const long long first = issued > kStages ? issued - kStages : 0;
+    for (long long j = first; j < issued; ++j) mbar_wait(&sm.full[int(j % kStages)], uint32_t(j / kStages) & 1);
+  }
 }
 
-// Combines the partial states of sequences split across CTAs:
-//   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  out = sum_c acc_c 2^(m_c - M) / L.
-// Also writes the zero rows of empty or invalid sequences.
-__global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const DecodeArgs a) {
-  const int s = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int h = tid >> 3, d0 = (tid & 7) * 8;
-  float *o = a.out + ((long long)s * kQHeads + h) * kHeadDim + d0;
-  const int ctx = __ldg(a.context_lens + s);
-  if (ctx <= 0 || ctx > a.max_context) {
-    reinterpret_cast<float4 *>(o)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4 *>(o)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
-  }
-  const int2 info = a.seq_info[s];
-  if (info.x == info.y) return;  // written directly by its only CTA
-  // CTAs between the first and the last may own no pages at all (more CTAs than
-  // pages); they left no partial and are skipped.
-  const long long T = a.meta[0];
-  const long long G = a.meta[1];
-  float M = -INFINITY;
-  for (int c = info.x; c <= info.y; ++c) {
-    if ((long long)c * T / G == (long long)(c + 1) * T / G) continue;
-    M = fmaxf(M, a.part_ml[((long long)c + s) * kQHeads + h].x);
-  }
-  float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int c = info.x; c <= info.y; ++c) {
-      if ((long long)c * T / G == (long long)(c + 1) * T / G) continue;
-      const long long slot = (long long)c + s;
-      const float2 ml = a.part_ml[slot * kQHeads + h];
-      const float wgt = exp2f(ml.x - M);
-      L += ml.y * wgt;
-      const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (slot * kQHeads + h) * kHeadDim + d0);
-      const float4 x0 = src[0], x1 = src[1];
-      r[0] += wgt * x0.x; r[1] += wgt * x0.y; r[2] += wgt * x0.z; r[3] += wgt * x0.w;
-      r[4] += wgt * x1.x; r[5] += wgt * x1.y; r[6] += wgt * x1.z; r[7] += wgt * x1.w;
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  reinterpret_cast<float4 *>(o)[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
-  reinterpret_cast<float4 *>(o)[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
-}
-
-
-struct WorkspaceLayout {
-  long long *meta;
-  float *part_acc;
-  float2 *part_ml;
-  int2 *seq_info;
-  size_t bytes;
-};
-
-// [meta: 16 B][partial accumulators][partial (m, l)][per-sequence CTA span]
-WorkspaceLayout layout_workspace(void *base, int num_seqs) {
-  const size_t slots = size_t(kMaxCtas) + size_t(num_seqs);
-  WorkspaceLayout L;
-  uint8_t *p = static_cast<uint8_t *>(base);
-  const size_t meta_bytes = 16;
-  const size_t acc_bytes = slots * kQHeads * kHeadDim * sizeof(float);
-  const size_t ml_bytes = slots * kQHeads * sizeof(float2);
-  L.meta = reinterpret_cast<long long *>(p);
-  L.part_acc = reinterpret_cast<float *>(p + meta_bytes);
-  L.part_ml = reinterpret_cast<float2 *>(p + meta_bytes + acc_bytes);
-  L.seq_info = reinterpret_cast<int2 *>(p + meta_bytes + acc_bytes + ml_bytes);
-  L.bytes = meta_bytes + acc_bytes + ml_bytes + size_t(num_seqs) * sizeof(int2);
-  return L;
-}
+// The workspace is an array of kMaxCtas + num_seqs slots.  Slot positions do not
+// depend on num_seqs, so the ticket counters (zero between calls) stay valid when
+// the batch size changes.
+size_t workspace_bytes(int num_seqs) { return (size_t(kMaxCtas) + size_t(num_seqs)) * sizeof(Slot); }
 
 int auto_ctas(int num_seqs, int max_context) {
   const int sms = device_sm_count();
@@ -512,9 +589,9 @@ EncodeTiledFn encode_tiled_fn() {
 int encode_half_pages(CUtensorMap *map, const void *base, long long page_stride, int num_pages) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (fn == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kBoxRows), cuuint64_t(num_pages)};
+  const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kKvHeads * kPageTokens), cuuint64_t(num_pages)};
   const cuuint64_t strides[2] = {cuuint64_t(kRowBytes), cuuint64_t(page_stride)};
-  const cuuint32_t box[3] = {cuuint32_t(kHeadDim), cuuint32_t(kBoxRows), 1u};
+  const cuuint32_t box[3] = {cuuint32_t(kHeadDim), cuuint32_t(kKvHeads * kPageTokens), 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -538,8 +615,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   if (!aligned16(q) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(out) & 7u) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_ALIGN;
-  const WorkspaceLayout L = layout_workspace(workspace, num_seqs);
-  if (workspace_bytes < L.bytes) return PKV_ERR_WORKSPACE;
+  if (workspace_bytes < pkv::workspace_bytes(num_seqs)) return PKV_ERR_WORKSPACE;
   rc = setup_kernel_attributes();
   if (rc != PKV_OK) return rc;
 
@@ -557,19 +633,13 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.num_seqs = num_seqs;
   a.max_context = max_context;
   a.scale_log2 = scale * kLog2e;
-  a.part_acc = L.part_acc;
-  a.part_ml = L.part_ml;
-  a.seq_info = L.seq_info;
-  a.meta = L.meta;
+  a.slots = static_cast<Slot *>(workspace);
   a.status = device_status;
 
+  a.exact_ctas = num_ctas > 0 ? 1 : 0;
   const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   paged_decode_partial_kernel<<<G, kThreads, kSmemBytes, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
-  // A single CTA covers every sequence whole and writes the output itself, but
-  // sequences with no pages still need their zero rows from the merge kernel.
-  paged_decode_merge_kernel<<<num_seqs, kMergeThreads, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
   return PKV_OK;
 }
@@ -579,7 +649,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
 
 extern "C" size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim) {
   if (num_seqs < 0 || num_q_heads != pkv::kQHeads || head_dim != pkv::kHeadDim) return 0;
-  return pkv::layout_workspace(nullptr, num_seqs).bytes;
+  return pkv::workspace_bytes(num_seqs);
 }
 
 extern "C" int pkv_decode_max_ctas(void) { return pkv::kMaxCtas; }
@@ -588,7 +658,7 @@ extern "C" int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int
   if (num_seqs < 0 || max_context < 0) return PKV_ERR_SHAPE;
   const int g = num_seqs == 0 ? 0 : pkv::auto_ctas(num_seqs, max_context);
   if (num_ctas) *num_ctas = g;
-  if (launches) *launches = num_seqs == 0 ? 0 : 2;
+  if (launches) *launches = num_seqs == 0 ? 0 : 1;
   return PKV_OK;
 }
 
@@ -613,18 +683,15 @@ extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out,
 // ---------------------------------------------------------------------------
 // Allocation-free variant.  The workspace of pkv_paged_decode_attention lives in
 // a fixed device array of this file, sized for PKV_NOALLOC_MAX_SEQS sequences,
-// for callers that cannot allocate device memory.  Its device address is looked
-// up once per device (cudaGetSymbolAddress on the first call with that device
-// current); the call then follows the regular path with that address as the
-// workspace.  No value in the array needs to start at zero: every partial state,
-// span and total the merge reads is written earlier in the same call.
+// for callers that cannot allocate device memory.  On the first call with a
+// device current, its device address is looked up (cudaGetSymbolAddress) and the
+// array is cleared once (the ticket counters must start at zero; every completed
+// call leaves them at zero again).  The call then follows the regular path with
+// that address as the workspace.
 namespace pkv {
 namespace {
 
-constexpr size_t kNoallocScratchBytes =
-    16 + (size_t(kMaxCtas) + PKV_NOALLOC_MAX_SEQS) * (size_t(kQHeads) * kHeadDim * sizeof(float) +
-                                                      size_t(kQHeads) * sizeof(float2)) +
-    size_t(PKV_NOALLOC_MAX_SEQS) * sizeof(int2);
+constexpr size_t kNoallocScratchBytes = (size_t(kMaxCtas) + PKV_NOALLOC_MAX_SEQS) * sizeof(Slot);
 
 }  // namespace
 }  // namespace pkv
@@ -634,7 +701,7 @@ static __device__ __align__(256) unsigned char pkv_noalloc_scratch[pkv::kNoalloc
 namespace pkv {
 namespace {
 
-// Device address of pkv_noalloc_scratch on the current device, or nullptr.
+// Device address of pkv_noalloc_scratch on the current device (cleared on first use), or nullptr.
 void *noalloc_scratch_address() {
   static std::mutex mu;
   static void *addr[64] = {nullptr};
@@ -647,6 +714,10 @@ void *noalloc_scratch_address() {
   if (addr[dev] == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, pkv_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (cudaMemset(p, 0, kNoallocScratchBytes) != cudaSuccess) {
       cudaGetLastError();
       return nullptr;
     }
@@ -666,8 +737,6 @@ extern "C" int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *o
   if (num_seqs <= 0) {
     return num_seqs < 0 ? PKV_ERR_SHAPE : PKV_OK;
   }
-  const size_t need = pkv::layout_workspace(nullptr, num_seqs).bytes;
-  if (need > pkv::kNoallocScratchBytes) return PKV_ERR_NOALLOC_LIMIT;
   void *scratch = pkv::noalloc_scratch_address();
   if (scratch == nullptr) return PKV_ERR_CUDA;
   return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,

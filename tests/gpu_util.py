@@ -52,7 +52,7 @@ class DeviceDecode:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev())
         self.bt = to_dev(np.ascontiguousarray(wl.block_tables))            # [S, L, B]
         self.lens = to_dev(wl.context_lens)
-        self.ws = torch.empty(pkv.decode_workspace_bytes(wl.num_seqs), dtype=torch.uint8, device=dev())
+        self.ws = pkv.decode_workspace(wl.num_seqs, device=dev())
         self.out = torch.empty(wl.num_seqs, wl.num_q_heads, wl.head_dim, dtype=torch.float32, device=dev())
         self.generate_on_device = generate_on_device
 

@@ -217,3 +217,23 @@ def test_bandwidth_config_full_size_sampled():
     U.assert_close(out[sample], ref[sample], "bandwidth sample")
     # every output is a convex combination of V rows: finite and inside [min V, max V] per row
     assert np.isfinite(out).all()
+
+
+def test_one_workspace_across_batch_sizes_and_splits():
+    """The merge counters live at fixed slot positions and are reset by the merging CTA, so one
+    zeroed workspace stays valid across calls with different batch sizes and CTA counts."""
+    import paged_kv_cache_180_gb300 as pkv
+    ws = pkv.decode_workspace(64, device=U.dev())
+    for seed, n, ctas in ((480, 64, 0), (481, 5, 300), (482, 40, 17), (483, 64, 1024), (484, 3, 0)):
+        wl = configs.ragged(seed=seed, num_seqs=n)
+        d = U.DeviceDecode(wl)
+        d.ws = ws
+        d.append_all()
+        out = d.attend(num_ctas=ctas).cpu().double().numpy()
+        ref, err, _ = oracle.decode_workload(wl)
+        U.assert_close(out, ref, f"batch {n}, ctas {ctas}")
+        assert d.status_value() == 0
+    # every completed call leaves the counters at zero
+    slot_bytes = 32 * 64 * 4 + 32 * 8 + 16
+    counters = ws.view(-1, slot_bytes)[:, slot_bytes - 16:slot_bytes - 12].contiguous().view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
