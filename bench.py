@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--ctas", type=int, default=0, help="CTAs of the split-context pass (0 = the library's choice)")
+    p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                   help="replay each step as a CUDA graph (auto: on for the launch-bound workloads)")
     return p.parse_args()
 
 
@@ -291,16 +293,25 @@ def run_native(args):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool_bytes = wl.num_pages * 32768
-    flush = None
+    flush_w = flush_r = None
     if pool_bytes < 2 * l2:
-        flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+        # Between steps: write a buffer twice the L2 size, then read another one, so
+        # the timed kernels start with none of their inputs (and no dirty lines) in L2.
+        flush_w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+        flush_r = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=dev)
 
-    def step(e_marks=None):
+    def flush():
+        if flush_w is not None:
+            flush_w.zero_()
+            flush_r.max()
+
+    def step(e_marks=None, attention_only=False):
         for layer in range(L):
             kn, vn, sn = dec[layer]
             if e_marks is not None:
                 e_marks[0].record(stream)
-            pkv.kv_append(pool, kn, vn, sn, status)
+            if not attention_only:
+                pkv.kv_append(pool, kn, vn, sn, status)
             if e_marks is not None:
                 e_marks[1].record(stream)
             pkv.paged_decode_attention(pool, out, q[layer], bt.view(-1)[layer * blocks:], stride, lens,
@@ -309,13 +320,27 @@ def run_native(args):
                 e_marks[2].record(stream)
                 e_marks = e_marks[3:]
 
+    use_graph = args.graph == "on" or (args.graph == "auto" and wl.name != "bandwidth")
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
+    graphs = None
+    if use_graph:
+        # whole step, and attention only (for the per-kernel roofline), each one graph
+        graphs = []
+        for attention_only in (False, True):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(attention_only=attention_only)
+            graphs.append(g)
+        for _ in range(3):
+            graphs[0].replay()
+            graphs[1].replay()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(dev)
 
-    # ---- timed region: device time of every step, per-kernel events on the launching stream ----
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
+    # ---- timed region: device time of every step, CUDA events on the launching stream ----
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -323,28 +348,44 @@ def run_native(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(steps):
-        if flush is not None:
-            flush.zero_()
-        step(ev[i])
-    torch.cuda.synchronize()
+    append_ms, attn_ms, step_ms = [], [], []
+    if graphs is None:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
+        for i in range(steps):
+            flush()
+            step(ev[i])
+        torch.cuda.synchronize()
+        for i in range(steps):
+            tot = 0.0
+            for layer in range(L):
+                e0, e1, e2 = ev[i][3 * layer:3 * layer + 3]
+                a_, b_ = e0.elapsed_time(e1), e1.elapsed_time(e2)
+                append_ms.append(a_)
+                attn_ms.append(b_ / 1.0)
+                tot += a_ + b_
+            step_ms.append(tot)
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * steps)]
+        for i in range(steps):
+            flush()
+            ev[i][0].record(stream)
+            graphs[0].replay()
+            ev[i][1].record(stream)
+        for i in range(steps):
+            flush()
+            ev[steps + i][0].record(stream)
+            graphs[1].replay()
+            ev[steps + i][1].record(stream)
+        torch.cuda.synchronize()
+        step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+        attn_ms = [ev[steps + i][0].elapsed_time(ev[steps + i][1]) / L for i in range(steps)]
+        append_ms = [max(0.0, step_ms[i] / L - attn_ms[i]) for i in range(steps)]
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
     time.sleep(0.25)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
-
-    append_ms, attn_ms, step_ms = [], [], []
-    for i in range(steps):
-        tot = 0.0
-        for layer in range(L):
-            e0, e1, e2 = ev[i][3 * layer:3 * layer + 3]
-            a, b = e0.elapsed_time(e1), e1.elapsed_time(e2)
-            append_ms.append(a)
-            attn_ms.append(b)
-            tot += a + b
-        step_ms.append(tot)
     ms = sum(step_ms) / steps
     t_dev = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -392,8 +433,8 @@ def run_native(args):
             e2e_step()
         ts = []
         for _ in range(e2e_steps):
-            if flush is not None:
-                flush.zero_()
+            if flush_w is not None:
+                flush()
                 torch.cuda.synchronize()
             t0 = time.perf_counter()
             e2e_step()
@@ -420,8 +461,10 @@ def run_native(args):
                        "context_lens": ("2048 each" if wl.name == "bandwidth" else "per workload"),
                        "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
                        "pool_pages": wl.num_pages, "parallelism": f"replicas x{world}",
-                       "l2": ("inputs larger than L2 (1 GiB pool)" if flush is None else
-                              "L2 flushed between steps (write of 2x L2)"),
+                       "l2": ("inputs larger than L2 (1 GiB pool)" if flush_w is None else
+                              "L2 flushed between steps (write of a 2x L2 buffer, then read of another)"),
+                       "timing": ("CUDA graph replay per step (whole step; attention-only graph for the "
+                                  "per-kernel figure)" if graphs is not None else "CUDA events around each kernel"),
                        "split_ctas": ctas},
             "seq_layers_per_s": round(world * wl.num_seqs * L / (ms_max * 1e-3), 1),
             "pct_of_peak": {"measured": round(100 * value / world / peak, 2),
@@ -432,10 +475,11 @@ def run_native(args):
                          "algorithmic_bytes_per_launch": attn_b, "avg_launch_us": round(attn_avg_s * 1e6, 3),
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
-            "kernel_us": {"kv_append": round(1e3 * sum(append_ms) / len(append_ms), 3),
+            "kernel_us": {("kv_append" if graphs is None else "kv_append (step minus attention)"):
+                          round(1e3 * sum(append_ms) / len(append_ms), 3),
                           "paged_decode_attention": round(1e3 * sum(attn_ms) / len(attn_ms), 3)},
             "clocks": clocks,
-            "gpu_launches": steps * L * (1 + attn_launches),
+            "gpu_launches": steps * L * (1 + attn_launches) + (steps * L * attn_launches if graphs is not None else 0),
             "e2e": e2e,
         }
     if world > 1:

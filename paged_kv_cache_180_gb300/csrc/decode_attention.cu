@@ -599,6 +599,45 @@ int encode_half_pages(CUtensorMap *map, const void *base, long long page_stride,
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// The two tensor maps of a pool, from a small cache keyed by the pool's addresses
+// and shape (encoding them costs host time on every call otherwise).
+int pool_tensor_maps(const pkv_pool *pool, CUtensorMap *tk, CUtensorMap *tv) {
+  struct Entry {
+    const void *k, *v;
+    long long stride;
+    int pages;
+    CUtensorMap mk, mv;
+  };
+  constexpr int kEntries = 16;
+  static std::mutex mu;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    const Entry &e = cache[i];
+    if (e.k == pool->k_base && e.v == pool->v_base && e.stride == pool->page_stride_bytes &&
+        e.pages == pool->num_pages) {
+      *tk = e.mk;
+      *tv = e.mv;
+      return PKV_OK;
+    }
+  }
+  Entry e;
+  e.k = pool->k_base;
+  e.v = pool->v_base;
+  e.stride = pool->page_stride_bytes;
+  e.pages = pool->num_pages;
+  int rc = encode_half_pages(&e.mk, pool->k_base, pool->page_stride_bytes, pool->num_pages);
+  if (rc == PKV_OK) rc = encode_half_pages(&e.mv, pool->v_base, pool->page_stride_bytes, pool->num_pages);
+  if (rc != PKV_OK) return rc;
+  cache[next] = e;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  *tk = e.mk;
+  *tv = e.mv;
+  return PKV_OK;
+}
+
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
            int64_t bt_stride, const int32_t *context_lens, int num_seqs, int max_context, float scale,
            void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream) {
@@ -620,9 +659,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   if (rc != PKV_OK) return rc;
 
   DecodeArgs a;
-  rc = encode_half_pages(&a.tmap_k, pool->k_base, pool->page_stride_bytes, pool->num_pages);
-  if (rc != PKV_OK) return rc;
-  rc = encode_half_pages(&a.tmap_v, pool->v_base, pool->page_stride_bytes, pool->num_pages);
+  rc = pool_tensor_maps(pool, &a.tmap_k, &a.tmap_v);
   if (rc != PKV_OK) return rc;
   a.num_pages = pool->num_pages;
   a.q = static_cast<const uint32_t *>(q);
