@@ -221,6 +221,72 @@ int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *out, const v
                                        const int32_t *context_lens, int num_seqs, int max_context,
                                        float scale, int32_t *device_status, void *stream);
 
+/* ---- host page allocator and continuous-batching scheduler (no GPU) --------------------
+ *
+ * Cited: samir-vllm README, "What works so far" (requests share the pool; static and
+ * continuous batching admit queued prompts by page budget and return pages and budgets on
+ * completion) and "Current scope" (admission credits = pages for prompt + new - 1 tokens,
+ * rounded up to 16-token pages, in every layer; the new-token budget is clamped to the
+ * context limit; credits are separate from pages, which are assigned lazily; FIFO waits;
+ * a request larger than the whole pool is rejected; --stats counters); tiny-vllm part 3,
+ * "Distributing K/V into paged blocks" (pages popped from the back of a free list when a
+ * block is first written; -1 marks an unassigned block).
+ *
+ * A step: (1) retire the requests that finished last step (their pages go back on the free
+ * list, block order per layer, and their credits are released); (2) admit queued requests
+ * in FIFO order into the lowest free slots while their credits fit (head-of-line blocking;
+ * a blocked head with a free slot counts one admission wait per step) and plan the append
+ * of their prompt tokens; (3) every active request with tokens left to decode appends one
+ * token (a just-admitted one included) and attends.  A request with prompt P and budget N
+ * decodes N - 1 tokens, so its context ends at P + N - 1.  Pages are taken from the back of
+ * the free list when a token is the first of its block, in every layer.
+ */
+typedef struct pkv_sched pkv_sched;
+
+typedef struct pkv_step_plan {
+    int32_t num_finished;              /* requests retired at the start of this step */
+    const int64_t *finished_request;   /* [num_finished] */
+    int32_t num_admitted;
+    const int64_t *admitted_request;   /* [num_admitted] */
+    const int32_t *admitted_slot;      /* [num_admitted] */
+    int32_t num_appends;               /* tokens to append: admitted prompts, then one per decoding slot */
+    const int64_t *append_request;     /* [num_appends] request of each token */
+    const int32_t *append_position;    /* [num_appends] absolute position of the token in its request */
+    const int32_t *append_slot_mapping;/* [num_layers][num_appends]: page * page_tokens + row */
+    int32_t num_decode;                /* slots that decode this step */
+    const int32_t *decode_slot;        /* [num_decode] ascending */
+    const int32_t *context_lens;       /* [num_slots]: context after this step's append, 0 if idle */
+    const int32_t *block_tables;       /* [num_slots][num_layers][max_blocks], -1 = unassigned */
+    int32_t max_blocks;                /* ceil(max_context / page_tokens) */
+} pkv_step_plan;
+
+typedef struct pkv_sched_stats {
+    int32_t pool_pages;
+    int32_t peak_active;       /* most requests holding a slot at once */
+    int32_t largest_batch;     /* most sequences decoding in one step */
+    int32_t peak_pages;        /* most pages assigned at once */
+    int32_t admission_waits;   /* steps in which the queue head waited for credits with a slot free */
+    int32_t free_pages;        /* pages on the free list now */
+    int32_t credits_in_use;
+    int32_t active;
+    int32_t queued;
+    int64_t steps;
+} pkv_sched_stats;
+
+/* free_order: host, nullable - initial free list (num_pages distinct ids, popped from the
+ * back); NULL means 0 .. num_pages-1.  Returns PKV_OK, PKV_ERR_NULL or PKV_ERR_SHAPE. */
+int pkv_sched_create(int num_pages, int num_layers, int page_tokens, int max_context, int num_slots,
+                     const int32_t *free_order, pkv_sched **out);
+void pkv_sched_destroy(pkv_sched *sched);
+/* Queue a request.  max_new_tokens is clamped so prompt + new - 1 <= max_context.
+ * PKV_ERR_EXCEEDS_POOL if its credits exceed the whole pool (it is not queued),
+ * PKV_ERR_SHAPE for prompt < 1, prompt > max_context or max_new_tokens < 1. */
+int pkv_sched_submit(pkv_sched *sched, int64_t request_id, int prompt_tokens, int max_new_tokens);
+/* Run one step and describe it in *plan (pointers stay valid until the next call).
+ * PKV_ERR_NO_PAGE if the free list ran dry (cannot happen while credits are honoured). */
+int pkv_sched_step(pkv_sched *sched, pkv_step_plan *plan);
+int pkv_sched_stats_get(const pkv_sched *sched, pkv_sched_stats *out);
+
 /* Short English text for a PKV_ERR_* code or PKV_OK. */
 const char *pkv_status_string(int status);
 

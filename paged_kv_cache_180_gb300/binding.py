@@ -38,6 +38,27 @@ class PkvPool(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class PkvStepPlan(ctypes.Structure):
+    """Mirror of ``pkv_step_plan``."""
+    _fields_ = [("num_finished", ctypes.c_int32), ("finished_request", ctypes.POINTER(ctypes.c_int64)),
+                ("num_admitted", ctypes.c_int32), ("admitted_request", ctypes.POINTER(ctypes.c_int64)),
+                ("admitted_slot", ctypes.POINTER(ctypes.c_int32)),
+                ("num_appends", ctypes.c_int32), ("append_request", ctypes.POINTER(ctypes.c_int64)),
+                ("append_position", ctypes.POINTER(ctypes.c_int32)),
+                ("append_slot_mapping", ctypes.POINTER(ctypes.c_int32)),
+                ("num_decode", ctypes.c_int32), ("decode_slot", ctypes.POINTER(ctypes.c_int32)),
+                ("context_lens", ctypes.POINTER(ctypes.c_int32)), ("block_tables", ctypes.POINTER(ctypes.c_int32)),
+                ("max_blocks", ctypes.c_int32)]
+
+
+class PkvSchedStats(ctypes.Structure):
+    """Mirror of ``pkv_sched_stats``."""
+    _fields_ = [("pool_pages", ctypes.c_int32), ("peak_active", ctypes.c_int32), ("largest_batch", ctypes.c_int32),
+                ("peak_pages", ctypes.c_int32), ("admission_waits", ctypes.c_int32), ("free_pages", ctypes.c_int32),
+                ("credits_in_use", ctypes.c_int32), ("active", ctypes.c_int32), ("queued", ctypes.c_int32),
+                ("steps", ctypes.c_int64)]
+
+
 _P, _I, _L, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 _PP = ctypes.POINTER(PkvPool)
 
@@ -53,6 +74,11 @@ EXPORTS = {
     "pkv_decode_plan": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_paged_decode_attention_noalloc": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _P]),
+    "pkv_sched_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
+    "pkv_sched_destroy": (None, [_P]),
+    "pkv_sched_submit": (_I, [_P, _L, _I, _I]),
+    "pkv_sched_step": (_I, [_P, ctypes.POINTER(PkvStepPlan)]),
+    "pkv_sched_stats_get": (_I, [_P, ctypes.POINTER(PkvSchedStats)]),
 }
 
 NOALLOC_MAX_SEQS = 512  # PKV_NOALLOC_MAX_SEQS
@@ -190,3 +216,60 @@ def paged_decode_attention_noalloc(pool: KVPool | PkvPool, out: torch.Tensor, q:
                                                  _ptr(block_tables), block_table_stride, _ptr(context_lens),
                                                  num_seqs, max_context, scale, _ptr(status), _stream(stream))
     _check("pkv_paged_decode_attention_noalloc", rc)
+
+
+class Scheduler:
+    """Host page allocator + continuous-batching scheduler of ``libpkv.so`` (see ``pkv_sched_*``)."""
+
+    def __init__(self, num_pages: int, num_layers: int = 1, page_tokens: int = 16, max_context: int = 2048,
+                 num_slots: int = 32, free_order=None):
+        import numpy as np
+        self._np = np
+        self.num_layers, self.num_slots = num_layers, num_slots
+        order = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            order = self._order.ctypes.data
+        h = ctypes.c_void_p()
+        _check("pkv_sched_create", _lib.pkv_sched_create(num_pages, num_layers, page_tokens, max_context, num_slots,
+                                                         order, ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.pkv_sched_destroy(h)
+            self._h = None
+
+    def submit(self, request_id: int, prompt_tokens: int, max_new_tokens: int) -> None:
+        _check("pkv_sched_submit", _lib.pkv_sched_submit(self._h, int(request_id), int(prompt_tokens),
+                                                         int(max_new_tokens)))
+
+    def step(self) -> dict:
+        """One step; returns copies of the plan as numpy arrays."""
+        np = self._np
+        plan = PkvStepPlan()
+        _check("pkv_sched_step", _lib.pkv_sched_step(self._h, ctypes.byref(plan)))
+
+        def arr(ptr, n, dt):
+            if n == 0:
+                return np.zeros(0, dtype=dt)
+            return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dt, copy=True)
+
+        na, L, S = plan.num_appends, self.num_layers, self.num_slots
+        return {
+            "finished": arr(plan.finished_request, plan.num_finished, np.int64),
+            "admitted": arr(plan.admitted_request, plan.num_admitted, np.int64),
+            "admitted_slot": arr(plan.admitted_slot, plan.num_admitted, np.int32),
+            "append_request": arr(plan.append_request, na, np.int64),
+            "append_position": arr(plan.append_position, na, np.int32),
+            "append_slot_mapping": arr(plan.append_slot_mapping, na * L, np.int32).reshape(L, na),
+            "decode_slot": arr(plan.decode_slot, plan.num_decode, np.int32),
+            "context_lens": arr(plan.context_lens, S, np.int32),
+            "block_tables": arr(plan.block_tables, S * L * plan.max_blocks, np.int32).reshape(S, L, plan.max_blocks),
+        }
+
+    def stats(self) -> dict:
+        st = PkvSchedStats()
+        _check("pkv_sched_stats_get", _lib.pkv_sched_stats_get(self._h, ctypes.byref(st)))
+        return {name: int(getattr(st, name)) for name, _ in PkvSchedStats._fields_}
