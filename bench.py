@@ -51,6 +51,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--ctas", type=int, default=0, help="CTAs of the split-context pass (0 = the library's choice)")
+    p.add_argument("--step", choices=["fused", "separate"], default="fused",
+                   help="fused: pkv_decode_step (append + attention in one launch); separate: kv_append, then "
+                        "paged_decode_attention")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step as a CUDA graph (auto: on for the launch-bound workloads)")
     return p.parse_args()
@@ -305,17 +308,26 @@ def run_native(args):
             flush_w.zero_()
             flush_r.max()
 
+    fused = args.step == "fused"
+
     def step(e_marks=None, attention_only=False):
         for layer in range(L):
             kn, vn, sn = dec[layer]
+            bt_l = bt.view(-1)[layer * blocks:]
             if e_marks is not None:
                 e_marks[0].record(stream)
-            if not attention_only:
-                pkv.kv_append(pool, kn, vn, sn, status)
-            if e_marks is not None:
-                e_marks[1].record(stream)
-            pkv.paged_decode_attention(pool, out, q[layer], bt.view(-1)[layer * blocks:], stride, lens,
-                                       wl.max_context, wl.scale, ws, status, num_ctas=args.ctas)
+            if fused and not attention_only:
+                if e_marks is not None:
+                    e_marks[1].record(stream)
+                pkv.decode_step(pool, kn, vn, sn, out, q[layer], bt_l, stride, lens, wl.max_context, wl.scale, ws,
+                                status)
+            else:
+                if not attention_only:
+                    pkv.kv_append(pool, kn, vn, sn, status)
+                if e_marks is not None:
+                    e_marks[1].record(stream)
+                pkv.paged_decode_attention(pool, out, q[layer], bt_l, stride, lens, wl.max_context, wl.scale, ws,
+                                           status, num_ctas=args.ctas)
             if e_marks is not None:
                 e_marks[2].record(stream)
                 e_marks = e_marks[3:]
@@ -396,7 +408,9 @@ def run_native(args):
     bytes_step = (attn_b + app_b) * L
     value = world * bytes_step / (ms_max * 1e-3) / 1e9
     attn_avg_s = (sum(attn_ms) / len(attn_ms)) * 1e-3
-    achieved = attn_b / attn_avg_s / 1e9
+    # dominant kernel: the fused step kernel (attention + append bytes) or the attention kernel
+    kernel_b = attn_b + app_b if (fused and graphs is None) else attn_b
+    achieved = kernel_b / attn_avg_s / 1e9
     peak, peak_kind = measured_peak()
 
     # ---- end to end through the public calls with host buffers ----
@@ -422,9 +436,14 @@ def run_native(args):
                 for dst, src in zip(d_dec[layer], h_dec[layer]):
                     dst.copy_(src, non_blocking=True)
                 kn, vn, sn = d_dec[layer]
-                pkv.kv_append(pool, kn, vn, sn, status)
-                pkv.paged_decode_attention(pool, out, d_q[layer], d_bt.view(-1)[layer * blocks:], stride, d_lens,
-                                           wl.max_context, wl.scale, ws, status, num_ctas=args.ctas)
+                bt_l = d_bt.view(-1)[layer * blocks:]
+                if fused:
+                    pkv.decode_step(pool, kn, vn, sn, out, d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                                    wl.scale, ws, status)
+                else:
+                    pkv.kv_append(pool, kn, vn, sn, status)
+                    pkv.paged_decode_attention(pool, out, d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                                               wl.scale, ws, status, num_ctas=args.ctas)
                 h_out.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -471,15 +490,20 @@ def run_native(args):
                             "nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
-                         "kernel": "paged_decode_attention call (split-context pass + merge)",
-                         "algorithmic_bytes_per_launch": attn_b, "avg_launch_us": round(attn_avg_s * 1e6, 3),
+                         "kernel": ("pkv_decode_step (append + split-context attention + merge, one launch)"
+                                    if (fused and graphs is None) else
+                                    "paged_decode_attention (split-context attention + merge, one launch)"),
+                         "algorithmic_bytes_per_launch": kernel_b, "avg_launch_us": round(attn_avg_s * 1e6, 3),
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
-            "kernel_us": {("kv_append" if graphs is None else "kv_append (step minus attention)"):
-                          round(1e3 * sum(append_ms) / len(append_ms), 3),
-                          "paged_decode_attention": round(1e3 * sum(attn_ms) / len(attn_ms), 3)},
+            "kernel_us": ({"decode_step": round(1e3 * sum(attn_ms) / len(attn_ms), 3)} if (fused and graphs is None)
+                          else {("kv_append" if graphs is None else "append (step minus attention)"):
+                                round(1e3 * sum(append_ms) / len(append_ms), 3),
+                                "paged_decode_attention": round(1e3 * sum(attn_ms) / len(attn_ms), 3)}),
+            "step_kind": args.step,
             "clocks": clocks,
-            "gpu_launches": steps * L * (1 + attn_launches) + (steps * L * attn_launches if graphs is not None else 0),
+            "gpu_launches": steps * L * ((0 if fused else 1) + attn_launches)
+                            + (steps * L * attn_launches if graphs is not None else 0),
             "e2e": e2e,
         }
     if world > 1:

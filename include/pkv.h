@@ -173,6 +173,26 @@ int pkv_paged_decode_attention(const pkv_pool *pool, float *out, const void *q, 
                                void *stream);
 
 /*
+ * pkv_decode_step - one decode step for num_seqs sequences in one launch: append each
+ * sequence's new token, then attend (pkv_kv_append followed by pkv_paged_decode_attention,
+ * fused).  k_new, v_new (device, bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned)
+ * hold sequence s's new token, which is position context_lens[s] - 1 (the last token
+ * attended); slot_mapping[s] (device int32) is that position's slot in the pool (it must lie
+ * in the last page of the sequence's block-table row); a negative slot means sequence s has
+ * no new token this step (its cached tokens are attended as they are).  The CTA that holds
+ * a sequence's last page takes the new token's rows straight from k_new/v_new and writes
+ * them to the pool.  A slot past the pool sets PKV_DEV_BAD_SLOT (the token is still
+ * attended, not stored).  A sequence with context 0 appends nothing.  Other arguments,
+ * errors and results are those of pkv_paged_decode_attention.
+ * Cited: samir-vllm README "What works so far" (decode appends one new token at its
+ * absolute position, then paged attention over the sequence's pages).
+ */
+int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                    float *out, const void *q, int num_q_heads, const int32_t *block_tables,
+                    int64_t block_table_stride, const int32_t *context_lens, int num_seqs, int max_context,
+                    float scale, void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/*
  * Same as pkv_paged_decode_attention with the number of CTAs of the split-context pass
  * fixed by the caller (1 .. pkv_decode_max_ctas(); 0 = automatic).  The result must not
  * depend on it beyond FP32 rounding; tests sweep it.

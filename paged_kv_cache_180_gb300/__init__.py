@@ -7,7 +7,7 @@ library with ``python -m paged_kv_cache_180_gb300.build``.
 The public names below load the binding on first use; if ``libpkv.so`` is
 missing that raises ImportError (there is no fallback path).
 """
-_PUBLIC = ("KVPool", "PkvError", "PkvPool", "decode_max_ctas", "decode_plan", "decode_workspace", "decode_workspace_bytes",
+_PUBLIC = ("KVPool", "PkvError", "PkvPool", "decode_max_ctas", "decode_plan", "decode_step", "decode_workspace", "decode_workspace_bytes",
            "kv_append", "kv_pool_bytes", "kv_pool_create", "paged_decode_attention",
            "paged_decode_attention_noalloc", "Scheduler", "status_string")
 

@@ -99,6 +99,16 @@ struct DecodeArgs {
   Slot *slots;       // [kMaxCtas + num_seqs] partial states and ticket counters
   int32_t *status;
   int exact_ctas;    // 1: split over exactly min(gridDim.x, T) CTAs (the caller chose the count)
+  // Fused append (pkv_decode_step), else null: sequence s's new token (position ctx-1)
+  // goes to slot_mapping[s]; its rows replace the stale ones of the last page in shared
+  // memory and are written to the pool by the CTA that holds that page.
+  const uint4 *k_new;  // [num_seqs][8][64] bf16, 8 uint4 per head row
+  const uint4 *v_new;
+  const int32_t *slot_mapping;
+  uint8_t *k_pool;     // pool bases for the write
+  uint8_t *v_pool;
+  long long page_stride;
+  long long num_slots;  // num_pages * 16
 };
 
 struct __align__(1024) Smem {
@@ -365,6 +375,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       aborted = true;
     }
     const int valid = min(kPageTokens, w.ctx - w.lp * kPageTokens);
+    if (a.slot_mapping != nullptr && w.lp == w.n - 1 && !aborted) {
+      // Fused append: the new token is the last of this page.  Lanes 0-7 move its K row of
+      // head g (16 B each), lanes 8-15 its V row, into the stage (swizzled position) and the pool.
+      const long long slot = __ldg(a.slot_mapping + w.s);
+      if (slot >= 0 && lane < 16) {
+        const int r = valid - 1, c = lane & 7, is_v = lane >> 3;
+        const uint4 x = __ldg((is_v ? a.v_new : a.k_new) + ((long long)w.s * kKvHeads + g) * 8 + c);
+        if (sm.stage_ok[st]) {
+          uint8_t *row = sm.kv[st][is_v] + (g * kPageTokens + r) * kRowBytes;
+          *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = x;
+        }
+        if (slot < a.num_slots) {
+          uint8_t *dst = (is_v ? a.v_pool : a.k_pool) + (slot / kPageTokens) * a.page_stride +
+                         (long long)(g * kPageTokens + slot % kPageTokens) * kRowBytes + c * 16;
+          *reinterpret_cast<uint4 *>(dst) = x;
+        } else if (g == 0 && lane == 0) {
+          report(a.status, PKV_DEV_BAD_SLOT);
+        }
+        fence_proxy_async_smem();  // these generic stores precede the stage's next TMA refill
+      }
+      __syncwarp();
+    }
     if (!aborted && sm.stage_ok[st]) {
       const uint32_t kbase = smem_addr(sm.kv[st][0]) + g * kHeadRowsBytes;
       const uint32_t vbase = smem_addr(sm.kv[st][1]) + g * kHeadRowsBytes;
@@ -435,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     __syncwarp();
     if (i + kStages < count) {
       if (lane == 0 && !aborted) {
+        if (a.slot_mapping != nullptr && w.lp == w.n - 1) __threadfence_block();  // after the fused-append stores
         const unsigned done = atomicAdd(&sm.stage_done[st], 1u) + 1u;
         if (done % kWarps == 0) {
           issue_page(a, sm, st, wi, policy);
@@ -640,7 +673,8 @@ int pool_tensor_maps(const pkv_pool *pool, CUtensorMap *tk, CUtensorMap *tv) {
 
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
            int64_t bt_stride, const int32_t *context_lens, int num_seqs, int max_context, float scale,
-           void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream) {
+           void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream,
+           const void *k_new = nullptr, const void *v_new = nullptr, const int32_t *slot_mapping = nullptr) {
   int rc = check_pool(pool);
   if (rc != PKV_OK) return rc;
   if (num_q_heads != kQHeads) return PKV_ERR_UNSUPPORTED;
@@ -674,6 +708,13 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.status = device_status;
 
   a.exact_ctas = num_ctas > 0 ? 1 : 0;
+  a.k_new = static_cast<const uint4 *>(k_new);
+  a.v_new = static_cast<const uint4 *>(v_new);
+  a.slot_mapping = slot_mapping;
+  a.k_pool = static_cast<uint8_t *>(pool->k_base);
+  a.v_pool = static_cast<uint8_t *>(pool->v_base);
+  a.page_stride = pool->page_stride_bytes;
+  a.num_slots = (long long)pool->num_pages * pool->page_tokens;
   const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   paged_decode_partial_kernel<<<G, kThreads, kSmemBytes, st>>>(a);
@@ -706,6 +747,20 @@ extern "C" int pkv_paged_decode_attention(const pkv_pool *pool, float *out, cons
                                           void *stream) {
   return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
                      max_context, scale, workspace, workspace_bytes, device_status, 0, stream);
+}
+
+extern "C" int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new,
+                               const int32_t *slot_mapping, float *out, const void *q, int num_q_heads,
+                               const int32_t *block_tables, int64_t block_table_stride, const int32_t *context_lens,
+                               int num_seqs, int max_context, float scale, void *workspace, size_t workspace_bytes,
+                               int32_t *device_status, void *stream) {
+  if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr)) return PKV_ERR_NULL;
+  if (num_seqs > 0 && (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) ||
+                       (reinterpret_cast<uintptr_t>(slot_mapping) & 3u)))
+    return PKV_ERR_ALIGN;
+  return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
+                     max_context, scale, workspace, workspace_bytes, device_status, 0, stream, k_new, v_new,
+                     slot_mapping);
 }
 
 extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out, const void *q, int num_q_heads,

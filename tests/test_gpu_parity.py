@@ -237,3 +237,50 @@ def test_one_workspace_across_batch_sizes_and_splits():
     slot_bytes = 32 * 64 * 4 + 32 * 8 + 16
     counters = ws.view(-1, slot_bytes)[:, slot_bytes - 16:slot_bytes - 12].contiguous().view(torch.int32)
     assert int(counters.abs().sum().item()) == 0
+
+
+# ---------------------------------------------------------------------------
+def _decode_step_case(wl, skip_every=0, layers=(0,)):
+    """Pool holds every token but each sequence's last; one fused step appends it and attends."""
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+    d = U.DeviceDecode(wl)
+    for layer in layers:
+        k, v, slots = torch_gen.workload_kv(wl, layer, U.dev(), upto_offset=1)
+        if slots.numel():
+            pkv.kv_append(d.pool, k, v, slots, d.status)
+    for layer in layers:
+        kn, vn, sn = wl.decode_tokens(layer)
+        sn = sn.copy()
+        if skip_every:
+            # these sequences' new tokens were appended earlier: slot -1 means "nothing to append"
+            pre = np.arange(0, len(sn), skip_every)
+            pkv.kv_append(d.pool, U.to_dev(kn[pre]), U.to_dev(vn[pre]), U.to_dev(sn[pre]), d.status)
+            sn[pre] = -1
+        blocks = wl.max_blocks
+        pkv.decode_step(d.pool, U.to_dev(kn), U.to_dev(vn), U.to_dev(sn), d.out, d.q(layer),
+                        d.bt.view(-1)[layer * blocks:], wl.num_layers * blocks, d.lens, wl.max_context, wl.scale,
+                        d.ws, d.status)
+        out = d.out.cpu().double().numpy()
+        ref, err, opool = oracle.decode_workload(wl, layer=layer)
+        assert err == 0
+        U.assert_close(out, ref, f"decode_step {wl.name} layer {layer}")
+    assert d.status_value() == 0
+    # the pool now equals the oracle's after appending every token of every layer
+    opool = oracle.Pool(wl.num_pages)
+    for layer in layers:
+        k, v, slots = wl.kv_all(layer)
+        oracle.kv_append(opool, k, v, slots)
+    np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), opool.data.reshape(-1))
+
+
+def test_decode_step_fused_append_ragged():
+    _decode_step_case(configs.ragged(seed=490, num_seqs=40))
+
+
+def test_decode_step_with_skipped_appends_and_partial_pages():
+    _decode_step_case(configs.custom(491, [1, 16, 17, 33, 2048, 300, 15, 32], name="fused_edges"), skip_every=3)
+
+
+def test_decode_step_llama_layers():
+    _decode_step_case(configs.llama_step(), layers=(0, 7, 15))
