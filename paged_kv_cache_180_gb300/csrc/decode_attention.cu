@@ -22,13 +22,14 @@
 //    sequence boundaries instead (a cut costs a merge), and no CTA gets fewer
 //    than 8 pages unless the caller fixes the count.  A sequence
 //    covered by one CTA is written out directly; a sequence cut across CTAs
-//    leaves one partial state (m, l, acc) per CTA in the workspace, and the
-//    last of those CTAs to finish (an atomic ticket on a counter, no waiting)
-//    merges them with the rule above: one launch per call.  The partial of
-//    (CTA c, sequence s) lives in slot c + s, unique because the (c, s) pairs
-//    of the list form a monotone staircase; the ticket counter of s lives in
-//    slot (first CTA of s) + s and is reset by the merging CTA, so a zeroed
-//    workspace stays valid across calls of any batch size.  Sequences with no
+//    leaves one partial state (m, l, acc) per CTA in the workspace, and for each
+//    group of 4 query heads the last warp to finish (an atomic ticket on a
+//    counter, no waiting, no CTA-wide barrier) merges them with the rule above:
+//    one launch per call.  The partial of (CTA c, sequence s) lives in slot
+//    c + s, unique because the (c, s) pairs of the list form a monotone
+//    staircase; the ticket counters of s live in slot (first CTA of s) + s and
+//    are reset by the merging warps, so a zeroed workspace stays valid across
+//    calls of any batch size.  Sequences with no
 //    pages (context 0 or invalid) get zero rows from CTA s % G.
 //  * Staging: each page arrives as two tiled TMA boxes (its K half and its V
 //    half: 8 heads x 16 tokens x 128 B rows, 16 KiB each, contiguous in the
@@ -80,8 +81,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Slot {
   float acc[kQHeads][kHeadDim];  // un-normalised sum of p * V
   float2 ml[kQHeads];            // (running max in log2 units, sum of p)
-  int counter;                   // CTAs of the sequence done so far; 0 between calls
-  int pad[3];
+  int counter[kWarps];           // per head group: CTAs of the sequence done so far; 0 between calls
 };
 
 struct DecodeArgs {
@@ -125,7 +125,6 @@ struct __align__(1024) Smem {
   long long seq0_first;  // global index of the first page of seq0
   int seq0;
   int found;
-  int merge_here;        // set when this CTA is the last to finish a cut sequence
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the dynamic base to 1024 B
 
@@ -251,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       sm.stage_done[i] = 0;
     }
     sm.found = 0;
-    sm.merge_here = 0;
     sm.issued = 0;
     sm.any_aborted = 0;
     mbar_init_fence();
@@ -501,25 +499,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
             *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
           if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
         }
-        // The barrier orders every warp's partial stores before thread 0's device-scope
-        // fence and ticket (release); thread 0 fences again after the ticket (acquire)
-        // before the barrier that lets the warps read the other CTAs' partials.
-        named_barrier_sync(1, kThreads);
-        // CTAs holding pages of this sequence: c_first .. c_last, less any with an empty range.
+        // Each warp settles its own query heads, without waiting for the other warps:
+        // __syncwarp orders the lanes' partial stores before lane 0's device-scope fence
+        // and ticket on the (sequence, head group) counter (release); lane 0 fences
+        // again after the ticket (acquire) before the lanes read the other CTAs' partials.
+        __syncwarp();
         const int c_first = cta_of_page(gfirst, T, Gu);
         const int c_last = cta_of_page(gfirst + w.n - 1, T, Gu);
-        if (tid == 0) {
+        int last = 0;
+        if (lane == 0) {
           const int parts = c_last - c_first + 1;  // every CTA in the span owns pages of it
-          int *counter = &a.slots[(long long)c_first + w.s].counter;
+          int *counter = &a.slots[(long long)c_first + w.s].counter[g];
           __threadfence();
           const int ticket = atomicAdd(counter, 1);
-          const int last = (ticket == parts - 1);
+          last = (ticket == parts - 1);
           if (last) atomicExch(counter, 0);  // ready for the next call
           __threadfence();
-          sm.merge_here = last;
         }
-        named_barrier_sync(1, kThreads);
-        if (sm.merge_here) {
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
           // warp g merges query heads 4g .. 4g+3: lane -> head 4g + lane/8, dims 8 (lane%8) .. +7
           const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
           float M = -INFINITY;

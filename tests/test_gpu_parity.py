@@ -234,8 +234,8 @@ def test_one_workspace_across_batch_sizes_and_splits():
         U.assert_close(out, ref, f"batch {n}, ctas {ctas}")
         assert d.status_value() == 0
     # every completed call leaves the counters at zero
-    slot_bytes = 32 * 64 * 4 + 32 * 8 + 16
-    counters = ws.view(-1, slot_bytes)[:, slot_bytes - 16:slot_bytes - 12].contiguous().view(torch.int32)
+    slot_bytes = 32 * 64 * 4 + 32 * 8 + 8 * 4
+    counters = ws.view(-1, slot_bytes)[:, slot_bytes - 32:].contiguous().view(torch.int32)
     assert int(counters.abs().sum().item()) == 0
 
 
