@@ -238,6 +238,64 @@ __device__ __forceinline__ void issue_page(const DecodeArgs &a, Smem &sm, int st
   }
 }
 
+// Warp g's share of finishing sequence s, cut across CTAs (its pages are the
+// global pages gfirst .. gfirst + n - 1), once this CTA's partial state is stored:
+// a ticket on the (sequence, head group) counter - an acquire-release atomic that
+// publishes the lanes' partial stores (ordered before it by __syncwarp) and, for
+// the last ticket, makes the other CTAs' partials visible.  ticket_of() takes the
+// ticket; merge_if_last() lets the warp holding the last ticket merge the partial
+// states of query heads 4g .. 4g+3 with
+//   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  out = sum_c acc_c 2^(m_c - M) / L
+// (one pass, rescaling as the running maximum grows) and reset the counter.  The
+// two halves may be apart: a warp can take the ticket, stream more pages, and only
+// then look at it.
+__device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long gfirst, int g, int lane, long long T,
+                                         int Gu) {
+  __syncwarp();
+  int ticket = 0;
+  if (lane == 0) ticket = atomic_add_acq_rel_gpu(&a.slots[(long long)cta_of_page(gfirst, T, Gu) + s].counter[g], 1);
+  return ticket;  // meaningful in lane 0
+}
+
+__device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long long gfirst, int n, int g, int lane,
+                                              long long T, int Gu, int ticket) {
+  const int c_first = cta_of_page(gfirst, T, Gu);
+  const int c_last = cta_of_page(gfirst + n - 1, T, Gu);
+  int last = 0;
+  if (lane == 0) {
+    last = (ticket == c_last - c_first);  // every CTA in the span owns pages of the sequence
+    if (last) atomicExch(&a.slots[(long long)c_first + s].counter[g], 0);  // ready for the next call
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __syncwarp();  // lane 0's acquire comes before every lane's reads of the partial states
+  // lane -> query head 4g + lane/8, dims 8 (lane%8) .. +7
+  const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
+  float M = -INFINITY, L = 0.f;
+  float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int c = c_first; c <= c_last; ++c) {
+    const Slot &part = a.slots[(long long)c + s];
+    const float2 ml = __ldcg(&part.ml[h]);
+    const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
+    const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+    // a part whose pages were all invalid has m = -inf and weight 0
+    const float m_new = fmaxf(M, ml.x);
+    const float keep = (m_new == -INFINITY) ? 1.f : exp2f(M - m_new);
+    const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - m_new);
+    L = L * keep + ml.y * wgt;
+    r[0] = r[0] * keep + wgt * x0.x; r[1] = r[1] * keep + wgt * x0.y;
+    r[2] = r[2] * keep + wgt * x0.z; r[3] = r[3] * keep + wgt * x0.w;
+    r[4] = r[4] * keep + wgt * x1.x; r[5] = r[5] * keep + wgt * x1.y;
+    r[6] = r[6] * keep + wgt * x1.z; r[7] = r[7] * keep + wgt * x1.w;
+    M = m_new;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float4 *dst = reinterpret_cast<float4 *>(a.out + ((long long)s * kQHeads + h) * kHeadDim + d0);
+  dst[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
+  dst[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
@@ -365,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   bool has_first = (w.lp == 0);
   long long gfirst = pa - w.lp;  // global index of the first page of the current sequence
   bool aborted = false;          // a wait gave up: stop waiting, computing and issuing, keep walking
+  int pend_s = -1, pend_n = 0, pend_ticket = 0;  // a cut sequence whose merge check waits for the end
+  long long pend_gfirst = 0;
 
   for (long long i = 0; i < count; ++i) {
     const int st = int(i % kStages);
@@ -473,6 +533,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
         }
       }
       wi.next(a);
+      // the walk ahead entered a new sequence: bring this warp's query rows of it into L2
+      if (wi.lp == 0 && lane < kGroup && wi.s < a.num_seqs)
+        prefetch_l2(a.q + ((long long)wi.s * kQHeads + g * kGroup + lane) * (kHeadDim / 2));
     }
     if (aborted && lane == 0) sm.any_aborted = 1;
 
@@ -499,49 +562,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
             *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
           if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
         }
-        // Each warp settles its own query heads, without waiting for the other warps:
-        // __syncwarp orders the lanes' partial stores before lane 0's device-scope fence
-        // and ticket on the (sequence, head group) counter (release); lane 0 fences
-        // again after the ticket (acquire) before the lanes read the other CTAs' partials.
-        __syncwarp();
-        const int c_first = cta_of_page(gfirst, T, Gu);
-        const int c_last = cta_of_page(gfirst + w.n - 1, T, Gu);
-        int last = 0;
-        if (lane == 0) {
-          const int parts = c_last - c_first + 1;  // every CTA in the span owns pages of it
-          int *counter = &a.slots[(long long)c_first + w.s].counter[g];
-          __threadfence();
-          const int ticket = atomicAdd(counter, 1);
-          last = (ticket == parts - 1);
-          if (last) atomicExch(counter, 0);  // ready for the next call
-          __threadfence();
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          // warp g merges query heads 4g .. 4g+3: lane -> head 4g + lane/8, dims 8 (lane%8) .. +7
-          const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
-          float M = -INFINITY;
-#pragma unroll 8
-          for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, __ldcg(&a.slots[(long long)c + w.s].ml[h]).x);
-          float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          float L = 0.f;
-          if (M != -INFINITY) {
-#pragma unroll 4
-            for (int c = c_first; c <= c_last; ++c) {
-              const Slot &part = a.slots[(long long)c + w.s];
-              const float2 ml = __ldcg(&part.ml[h]);
-              const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
-              const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
-              const float wgt = exp2f(ml.x - M);
-              L += ml.y * wgt;
-              r[0] += wgt * x0.x; r[1] += wgt * x0.y; r[2] += wgt * x0.z; r[3] += wgt * x0.w;
-              r[4] += wgt * x1.x; r[5] += wgt * x1.y; r[6] += wgt * x1.z; r[7] += wgt * x1.w;
-            }
-          }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          float4 *dst = reinterpret_cast<float4 *>(a.out + ((long long)w.s * kQHeads + h) * kHeadDim + d0);
-          dst[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
-          dst[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+        const int ticket = ticket_of(a, w.s, gfirst, g, lane, T, Gu);
+        if (has_first || i == count - 1) {
+          merge_if_last(a, w.s, gfirst, w.n, g, lane, T, Gu, ticket);
+        } else {
+          // The range began inside this sequence: look at the ticket after the loop,
+          // so its round trip (and a merge) do not stall the pages that follow.
+          pend_s = w.s;
+          pend_gfirst = gfirst;
+          pend_n = w.n;
+          pend_ticket = ticket;
         }
       }
       if (i + 1 < count) {
@@ -558,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       w.next(a);
     }
   }
+  if (pend_s >= 0) merge_if_last(a, pend_s, pend_gfirst, pend_n, g, lane, T, Gu, pend_ticket);
   named_barrier_sync(1, kThreads);
   if (tid == 0 && sm.any_aborted) {
     // Copies issued for pages nobody consumed: wait (bounded) so none lands after exit.

@@ -145,6 +145,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Device-scope atomic add with acquire-release semantics: this thread's earlier
+// writes (and those ordered before them) are visible before the add, and later
+// reads see what was visible to the writers whose adds it follows.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Fetch the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // L2 policy for data read exactly once per call (K/V pages): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
