@@ -59,6 +59,24 @@ def parse_args():
     return p.parse_args()
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's); the value
+    itself when not distributed.  Works with NCCL (CUDA tensor) and gloo (CPU tensor)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the workload (no data-path
+    exchange), so the job moves world x the bytes in the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
+
+
 def make_workload(name: str):
     from workloads import configs
     return configs.CONFIGS[name]()
@@ -399,14 +417,11 @@ def run_native(args):
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
     ms = sum(step_ms) / steps
-    t_dev = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_dev, op=dist.ReduceOp.MAX)
-    ms_max = float(t_dev.item())
+    ms_max = max_over_ranks(ms, dev)
 
     attn_b, app_b = step_bytes(wl)
     bytes_step = (attn_b + app_b) * L
-    value = world * bytes_step / (ms_max * 1e-3) / 1e9
+    value = whole_job_gbs(bytes_step, world, ms_max)
     attn_avg_s = (sum(attn_ms) / len(attn_ms)) * 1e-3
     # dominant kernel: the fused step kernel (attention + append bytes) or the attention kernel
     kernel_b = attn_b + app_b if (fused and graphs is None) else attn_b
@@ -458,12 +473,10 @@ def run_native(args):
             t0 = time.perf_counter()
             e2e_step()
             ts.append(time.perf_counter() - t0)
-        t_e2e = torch.tensor([sum(ts) / len(ts)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-        e2e = {"value": round(world * bytes_step / float(t_e2e.item()) / 1e9, 3), "unit": "GB/s",
+        t_e2e = max_over_ranks(sum(ts) / len(ts), dev)
+        e2e = {"value": round(whole_job_gbs(bytes_step, world, t_e2e * 1e3), 3), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(float(t_e2e.item()) * 1e3, 4),
+               "ms_per_step": round(t_e2e * 1e3, 4),
                "how": "host wall clock per step: pinned H2D of q, new K/V, slots, tables, lengths; append + "
                       "attention; D2H of the output; stream synchronize"}
 
