@@ -47,7 +47,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny"], default="bandwidth")
+    p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny", "trace"], default="bandwidth")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--ctas", type=int, default=0, help="CTAs of the split-context pass (0 = the library's choice)")
@@ -530,10 +530,140 @@ def run_native(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+def run_trace(args):
+    """Continuous-batching trace: 32 slots, 1 layer, 1000 steps planned by the library's
+    scheduler (prompts U[16, 512], new-token budgets U[1, 512], 4096-page pool).  Each step
+    appends its tokens (admitted prompts + one per decoding slot) and attends over every slot.
+    Plans and inputs are prepared before timing; each step's device time is taken with CUDA
+    events after an L2 flush (write of a 2x L2 buffer, then read of another)."""
+    import torch
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import configs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tr = configs.trace()
+    steps = min(args.steps if args.steps is not None else tr.num_steps, tr.num_steps)
+    warmup = args.warmup if args.warmup is not None else 3
+
+    sched = pkv.Scheduler(tr.num_pages, 1, 16, tr.max_context, tr.num_slots, tr.free_order)
+    for rid in range(tr.num_requests):
+        sched.submit(rid, int(tr.prompt_lens[rid]), int(tr.new_budgets[rid]))
+    t0 = time.perf_counter()
+    plans = [sched.step() for _ in range(steps)]
+    host_plan_us = (time.perf_counter() - t0) / steps * 1e6
+    stats = sched.stats()
+
+    # device inputs of every step
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    per_step = []
+    attn_bytes = app_bytes = seq_layers = 0
+    for i, pl in enumerate(plans):
+        reqs, pos = pl["append_request"], pl["append_position"]
+        ks, vs, j = [], [], 0
+        while j < len(reqs):
+            e = j
+            while e + 1 < len(reqs) and reqs[e + 1] == reqs[j] and pos[e + 1] == pos[e] + 1:
+                e += 1
+            k, v = tr.request_kv(int(reqs[j]), int(pos[j]), int(pos[e]) + 1)
+            ks.append(k)
+            vs.append(v)
+            j = e + 1
+        lens = pl["context_lens"]
+        q = np.zeros((tr.num_slots, 32, 64), np.uint16)
+        if len(pl["decode_slot"]):
+            q[pl["decode_slot"]] = tr.step_q(i, pl["decode_slot"])
+        bt = np.ascontiguousarray(pl["block_tables"][:, 0, :])
+        n_app = len(reqs)
+        per_step.append(dict(
+            k=to_dev(np.concatenate(ks)) if n_app else None, v=to_dev(np.concatenate(vs)) if n_app else None,
+            slots=to_dev(pl["append_slot_mapping"][0]) if n_app else None, q=to_dev(q), bt=to_dev(bt),
+            lens=to_dev(lens)))
+        live = lens > 0
+        attn_bytes += int(lens.sum()) * 2048 + int(live.sum()) * 4096 + 4 * int(np.ceil(lens[live] / 16).sum()) \
+            + 4 * tr.num_slots
+        app_bytes += n_app * APPEND_BYTES_PER_TOKEN
+        seq_layers += int(live.sum())
+    pool = pkv.KVPool(tr.num_pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pkv.decode_workspace(tr.num_slots, device=dev)
+    out = torch.empty(tr.num_slots, 32, 64, dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run_step(x):
+        if x["k"] is not None:
+            pkv.kv_append(pool, x["k"], x["v"], x["slots"], status)
+        pkv.paged_decode_attention(pool, out, x["q"], x["bt"], x["bt"].shape[1], x["lens"], tr.max_context, 0.125,
+                                   ws, status)
+
+    for x in per_step[:warmup]:       # warm-up on the first steps (replayed again below)
+        run_step(x)
+    pool.buffer.zero_()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in per_step]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    tw0 = time.time()
+    for x, (e0, e1) in zip(per_step, ev):
+        flush_w.zero_()
+        flush_r.max()
+        e0.record(stream)
+        run_step(x)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    value = whole_job_gbs(attn_bytes + app_bytes, world, total_ms)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/out",
+                "data": "synthetic (seeded N(0,1) bf16; seeded request trace)",
+                "config": {"workload": "trace", "slots": tr.num_slots, "layers": 1, "pool_pages": tr.num_pages,
+                           "requests": tr.num_requests, "prompt": "U[16, 512]", "new_tokens": "U[1, 512]",
+                           "parallelism": f"replicas x{world}",
+                           "l2": "L2 flushed before every step (write of a 2x L2 buffer, then read of another)",
+                           "timing": "CUDA events around each step's append + attention"},
+                "seq_layers_per_s": round(world * seq_layers / (total_ms * 1e-3), 1),
+                "host_plan_us_per_step": round(host_plan_us, 2),
+                "scheduler_stats": stats,
+                "clocks": sampler.summary(tw0, tw1),
+                "gpu_launches": sum((1 if x["k"] is not None else 0) + 1 for x in per_step)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.config == "trace":
+        return run_trace(args)
     return run_native(args)
 
 
