@@ -55,6 +55,9 @@ def _load(path: str):
     L.oracle_attention_weights.argtypes = [_P, _L, _I, _I, _I, _I, _P, _I, _P, _L, _P, _I, _I,
                                            _D, _P]
     L.oracle_attention_weights.restype = _I
+    L.oracle_paged_prefill_attention.argtypes = [_P, _P, _L, _I, _I, _I, _I, _P, _I, _P, _P, _L, _P, _I, _I, _D,
+                                                 _P]
+    L.oracle_paged_prefill_attention.restype = _I
     return L
 
 
@@ -148,6 +151,27 @@ def attention_weights(pool: Pool, q: np.ndarray, block_tables: np.ndarray, conte
                                          pool.num_kv_heads, head_dim, _ptr(q), num_q_heads, _ptr(bt),
                                          bt_stride, _ptr(lens), seq, head, float(scale), _ptr(w))
     return w, err
+
+
+def paged_prefill_attention(pool: Pool, q: np.ndarray, query_start: np.ndarray, block_tables: np.ndarray,
+                            context_lens: np.ndarray, scale: float, max_context: int, bt_stride: int | None = None):
+    """Causal attention of the last n_s tokens of each sequence (q rows query_start[s] .. query_start[s+1]-1).
+
+    Returns (out float64 [total, num_q_heads, head_dim], error bits)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    total, num_q_heads, head_dim = q.shape
+    if bt_stride is None:
+        bt_stride = int(bt.shape[-1])
+    out = np.zeros((total, num_q_heads, head_dim), dtype=np.float64)
+    kp, vp = pool._kv_ptrs()
+    err = lib().oracle_paged_prefill_attention(kp, vp, pool.page_stride, pool.num_pages, pool.page_tokens,
+                                               pool.num_kv_heads, head_dim, _ptr(q), num_q_heads, _ptr(qs), _ptr(bt),
+                                               bt_stride, _ptr(lens), int(lens.shape[0]), max_context, float(scale),
+                                               _ptr(out))
+    return out, err
 
 
 def decode_workload(wl, layer: int = 0, seqs=None, pool: Pool | None = None):

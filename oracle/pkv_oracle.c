@@ -223,3 +223,73 @@ int oracle_attention_weights(const uint16_t *k_pool, int64_t page_stride, int nu
     free(x);
     return bad ? ORACLE_ERR_PAGE : 0;
 }
+
+/*
+ * Paged prefill (and chunked prefill) attention: the query tokens of each sequence are
+ * the last n_s of its context_lens[s] tokens; query j of sequence s sits at position
+ * p = context_lens[s] - n_s + j and attends causally over tokens 0 .. p:
+ *   out[i][h][:] = sum_{t <= p} w_t V_t[h / group][:],  w = softmax_t(scale * q[i][h] . K_t[h / group])
+ * (the prefill path of "tiny-vllm part 3": per-head scores, causal mask keeping the
+ * diagonal, softmax, scores x V - here reading K/V through the block table).
+ * Query rows of sequence s are query_start[s] .. query_start[s+1]-1 of q
+ * ([total][num_q_heads][head_dim] bf16); out is FP64 [total][num_q_heads][head_dim].
+ * A sequence with n_s > context_lens[s], a context outside [0, max_context] or an
+ * invalid page gets zero rows and an error bit.
+ */
+int oracle_paged_prefill_attention(const uint16_t *k_pool, const uint16_t *v_pool, int64_t page_stride,
+                                   int num_pages, int page_tokens, int num_kv_heads, int head_dim,
+                                   const uint16_t *q, int num_q_heads, const int32_t *query_start,
+                                   const int32_t *block_tables, int64_t bt_stride, const int32_t *context_lens,
+                                   int num_seqs, int max_context, double scale, double *out)
+{
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        page_tokens <= 0 || num_seqs < 0 || max_context < 0)
+        return ORACLE_ERR_ARGS;
+    int group = num_q_heads / num_kv_heads;
+    int err = 0;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(max_context > 0 ? max_context : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(max_context > 0 ? max_context : 1));
+    for (int s = 0; s < num_seqs; ++s) {
+        int q0 = query_start[s], n = query_start[s + 1] - query_start[s];
+        int ctx = context_lens[s];
+        double *o_seq = out + (int64_t)q0 * num_q_heads * head_dim;
+        for (int64_t i = 0; i < (int64_t)n * num_q_heads * head_dim; ++i)
+            o_seq[i] = 0.0;
+        if (n <= 0)
+            continue;
+        if (ctx < 0 || ctx > max_context || n > ctx) {
+            err |= ORACLE_ERR_CONTEXT;
+            continue;
+        }
+        const int32_t *row = block_tables + (int64_t)s * bt_stride;
+        int bad = 0;
+        for (int j = 0; j < n && !bad; ++j) {
+            int pos = ctx - n + j;
+            for (int h = 0; h < num_q_heads; ++h) {
+                int g = h / group;
+                const uint16_t *qh = q + ((int64_t)(q0 + j) * num_q_heads + h) * head_dim;
+                if (head_scores(k_pool, page_stride, num_pages, page_tokens, head_dim, qh, g, row, pos + 1, scale,
+                                x)) {
+                    bad = 1;
+                    break;
+                }
+                softmax_weights(x, pos + 1, w);
+                double *o = o_seq + ((int64_t)j * num_q_heads + h) * head_dim;
+                for (int t = 0; t <= pos; ++t) {
+                    int64_t page = token_page(row, t, page_tokens, num_pages);
+                    int64_t v0 = element_index(page_stride, page, g, t % page_tokens, page_tokens, head_dim);
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += w[t] * bf16_value(v_pool[v0 + d]);
+                }
+            }
+        }
+        if (bad) {
+            err |= ORACLE_ERR_PAGE;
+            for (int64_t i = 0; i < (int64_t)n * num_q_heads * head_dim; ++i)
+                o_seq[i] = 0.0;
+        }
+    }
+    free(x);
+    free(w);
+    return err;
+}
