@@ -193,6 +193,34 @@ int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, 
                     float scale, void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
 
 /*
+ * pkv_paged_prefill_attention - causal attention of a chunk of query tokens per sequence
+ * over its paged K/V (prefill, chunked prefill; one query per sequence is decode).
+ *
+ *   out[i][h][:] = sum_{t <= p_i} w_t V_t[h / group][:],
+ *   w = softmax_{t <= p_i}( scale * q[i][h] . K_t[h / group] ),
+ *   p_i = context_lens[s] - n_s + (i - query_start[s])   for query row i of sequence s,
+ *   n_s = query_start[s+1] - query_start[s]: the queries are the last n_s cached tokens
+ *   (append them with pkv_kv_append first).
+ *
+ *   out            device; float32 [total][num_q_heads][head_dim], total = query_start[num_seqs].
+ *   q              device; bf16 [total][num_q_heads][head_dim], 16-byte aligned.
+ *   query_start    device; int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
+ *   block_tables, block_table_stride, context_lens, max_context: as for decode.
+ *   max_query      host bound on every n_s (sizes the grid; longer runs are not computed).
+ * A sequence with n_s > context_lens[s] or an invalid context gets zero rows and
+ * PKV_DEV_BAD_CONTEXT; an invalid page id inside a query's span sets PKV_DEV_BAD_PAGE
+ * (that page is left out).  No workspace.  One kernel launch.
+ * Cited: tiny-vllm part 3, "Per-head attention scores and GQA" and "causalMask and online
+ * softmax" (per-head scores, causal mask keeping the diagonal, softmax, scores x V), with
+ * K/V read through the block table as in "Distributing K/V into paged blocks".
+ */
+int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                const int32_t *query_start, const int32_t *block_tables,
+                                int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
+                                int max_query, int max_context, float scale, int32_t *device_status,
+                                void *stream);
+
+/*
  * Same as pkv_paged_decode_attention with the number of CTAs of the split-context pass
  * fixed by the caller (1 .. pkv_decode_max_ctas(); 0 = automatic).  The result must not
  * depend on it beyond FP32 rounding; tests sweep it.

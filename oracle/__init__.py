@@ -186,7 +186,7 @@ def decode_workload(wl, layer: int = 0, seqs=None, pool: Pool | None = None):
     chosen = range(wl.num_seqs) if seqs is None else seqs
     for s in chosen:
         c = int(wl.context_lens[s])
-        if c <= 0:
+        if c <= 0 or c > wl.max_blocks * wl.page_tokens:
             continue
         k, v = wl.kv_tokens(s, layer)
         kv_append(pool, k, v, wl.slot_mapping(s, layer, 0, c))

@@ -624,82 +624,6 @@ int setup_kernel_attributes() {
   return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
-
-// Tensor map of the K (or V) halves of a pool: element (d, row, page) with row =
-// kv_head * 16 + token, row stride 128 B, page stride page_stride_bytes; one box
-// is a whole half page (64 x 128 x 1), delivered 128-byte swizzled.
-int encode_half_pages(CUtensorMap *map, const void *base, long long page_stride, int num_pages) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (fn == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kKvHeads * kPageTokens), cuuint64_t(num_pages)};
-  const cuuint64_t strides[2] = {cuuint64_t(kRowBytes), cuuint64_t(page_stride)};
-  const cuuint32_t box[3] = {cuuint32_t(kHeadDim), cuuint32_t(kKvHeads * kPageTokens), 1u};
-  const cuuint32_t estride[3] = {1u, 1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
-}
-
-// The two tensor maps of a pool, from a small cache keyed by the pool's addresses
-// and shape (encoding them costs host time on every call otherwise).
-int pool_tensor_maps(const pkv_pool *pool, CUtensorMap *tk, CUtensorMap *tv) {
-  struct Entry {
-    const void *k, *v;
-    long long stride;
-    int pages;
-    CUtensorMap mk, mv;
-  };
-  constexpr int kEntries = 16;
-  static std::mutex mu;
-  static Entry cache[kEntries];
-  static int used = 0, next = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < used; ++i) {
-    const Entry &e = cache[i];
-    if (e.k == pool->k_base && e.v == pool->v_base && e.stride == pool->page_stride_bytes &&
-        e.pages == pool->num_pages) {
-      *tk = e.mk;
-      *tv = e.mv;
-      return PKV_OK;
-    }
-  }
-  Entry e;
-  e.k = pool->k_base;
-  e.v = pool->v_base;
-  e.stride = pool->page_stride_bytes;
-  e.pages = pool->num_pages;
-  int rc = encode_half_pages(&e.mk, pool->k_base, pool->page_stride_bytes, pool->num_pages);
-  if (rc == PKV_OK) rc = encode_half_pages(&e.mv, pool->v_base, pool->page_stride_bytes, pool->num_pages);
-  if (rc != PKV_OK) return rc;
-  cache[next] = e;
-  next = (next + 1) % kEntries;
-  if (used < kEntries) ++used;
-  *tk = e.mk;
-  *tv = e.mv;
-  return PKV_OK;
-}
-
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
            int64_t bt_stride, const int32_t *context_lens, int num_seqs, int max_context, float scale,
            void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream,
@@ -722,7 +646,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   if (rc != PKV_OK) return rc;
 
   DecodeArgs a;
-  rc = pool_tensor_maps(pool, &a.tmap_k, &a.tmap_v);
+  rc = pool_tensor_maps(pool, kKvHeads * kPageTokens, &a.tmap_k, &a.tmap_v);
   if (rc != PKV_OK) return rc;
   a.num_pages = pool->num_pages;
   a.q = static_cast<const uint32_t *>(q);

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the C-ABI translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,5 +30,9 @@ inline int check_pool(const pkv_pool *pool) {
 
 // Number of SMs of the current device (cached per device); 0 if it cannot be queried.
 int device_sm_count();
+
+// TMA tensor maps of the K and V halves of a checked pool, for boxes of box_rows
+// 128-byte rows of one page (128B swizzle); cached per pool.  PKV_OK or an error.
+int pool_tensor_maps(const pkv_pool *pool, int box_rows, CUtensorMap *tk, CUtensorMap *tv);
 
 }  // namespace pkv

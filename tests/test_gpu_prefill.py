@@ -1,0 +1,95 @@
+"""GPU parity of paged prefill attention (through the C ABI) against the oracle.
+
+Full prefills (the whole context is the query chunk), chunked prefills (a cached
+prefix plus a chunk), single queries (decode through the prefill entry point),
+ragged mixes in one launch, lengths not multiples of the 32-token tile or the
+16-token page, stale NaN bytes past each context, invalid sequences, the first query
+of a fresh prefill returning V[0] exactly, and page-permutation bit-exactness.
+Tolerance |gpu - oracle| <= 1e-3 + 1e-2 |oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import gpu_util as U
+from workloads import configs, rng
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _run(wl, nq, seed=1, bt=None):
+    """Queries = the last nq[s] tokens of each sequence (all already appended)."""
+    import paged_kv_cache_180_gb300 as pkv
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    total = int(qs[-1])
+    qbits = rng.normal_bf16(rng.stream_key(seed, "pf-q"), 0, total * 32 * 64).reshape(total, 32, 64)
+    out = torch.full((max(total, 1), 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
+    bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :] if bt is None else bt)
+    pkv.paged_prefill_attention(d.pool, out, U.to_dev(qbits), U.to_dev(qs), U.to_dev(bt_host), bt_host.shape[1],
+                                d.lens, max(max(nq), 1), wl.max_context, wl.scale, d.status)
+    got = out[:total].cpu().double().numpy()
+    opool = oracle.Pool(wl.num_pages)
+    k, v, slots = wl.kv_all(0)
+    oracle.kv_append(opool, k, v, slots)
+    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    return got, ref, err, d.status_value(), qs
+
+
+def test_full_prefills():
+    wl = configs.custom(600, [512, 17, 64, 100, 1], name="full")
+    nq = [512, 17, 64, 100, 1]
+    got, ref, err, st, _ = _run(wl, nq)
+    assert err == 0 and st == 0
+    U.assert_close(got, ref, "full prefill")
+
+
+def test_chunked_prefills_and_single_queries():
+    wl = configs.custom(601, [2048, 700, 33, 1000, 16, 5], name="chunked")
+    nq = [128, 1, 33, 77, 16, 2]
+    got, ref, err, st, _ = _run(wl, nq)
+    assert err == 0 and st == 0
+    U.assert_close(got, ref, "chunked prefill")
+
+
+def test_llama_prompt_shapes():
+    # prompts of the Llama step: 4 sequences, the whole context as the chunk (ctx up to 2048)
+    wl = configs.custom(602, [128, 512, 1024, 2048], name="llama_prefill")
+    got, ref, err, st, _ = _run(wl, [128, 512, 1024, 2048])
+    assert err == 0 and st == 0
+    U.assert_close(got, ref, "llama prompts")
+
+
+def test_first_query_of_fresh_prefill_is_v0_exactly():
+    wl = configs.custom(603, [40, 3], name="v0")
+    got, ref, err, st, qs = _run(wl, [40, 3])
+    for s in range(2):
+        _, v = wl.kv_tokens(s)
+        want = np.repeat(rng.bf16_bits_to_f64(v[0]), 4, axis=0).astype(np.float32)
+        assert np.array_equal(got[qs[s]].astype(np.float32), want)
+
+
+def test_invalid_sequences():
+    wl = configs.custom(604, [10, 30, 2049], num_pages=8, name="bad")
+    got, ref, err, st, qs = _run(wl, [11, 4, 3])    # 11 queries > 10 cached; 2049 > max_context
+    assert st == 2
+    assert not got[:11].any() and not got[15:].any()
+    U.assert_close(got[11:15], ref[11:15], "valid sequence beside invalid ones")
+
+
+def test_page_permutation_bit_exact():
+    wl = configs.custom(605, [300, 90], name="perm")
+    got1, _, _, _, _ = _run(wl, [60, 90])
+    perm = rng.permutation(rng.stream_key(606, "move"), wl.num_pages)
+    bt2 = np.where(wl.block_tables >= 0, perm[np.maximum(wl.block_tables, 0)], -1).astype(np.int32)
+    wl2 = configs.DecodeWorkload(wl.name, wl.seed, wl.num_pages, 1, wl.context_lens, bt2)
+    got2, _, _, _, _ = _run(wl2, [60, 90])
+    assert np.array_equal(got1.astype(np.float32).view(np.int32), got2.astype(np.float32).view(np.int32))

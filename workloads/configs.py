@@ -75,6 +75,11 @@ class DecodeWorkload:
     def token_elems(self) -> int:
         return self.num_kv_heads * self.head_dim
 
+    def has_pages(self, seq: int) -> bool:
+        """False for a context length outside [0, max_blocks * page_tokens] (edge-case tests): no pages."""
+        c = int(self.context_lens[seq])
+        return 0 <= c <= self.max_blocks * self.page_tokens
+
     def pages_used(self) -> int:
         return int(sum(math.ceil(int(c) / self.page_tokens) for c in self.context_lens)) * self.num_layers
 
@@ -104,7 +109,7 @@ class DecodeWorkload:
         ks, vs, slots = [], [], []
         for s in range(self.num_seqs):
             n = int(self.context_lens[s]) - upto_offset
-            if n <= 0:
+            if n <= 0 or not self.has_pages(s):
                 continue
             k, v = self.kv_tokens(s, layer, 0, n)
             ks.append(k)
@@ -120,7 +125,7 @@ class DecodeWorkload:
         ks, vs, slots = [], [], []
         for s in range(self.num_seqs):
             c = int(self.context_lens[s])
-            if c <= 0:
+            if c <= 0 or not self.has_pages(s):
                 continue
             k, v = self.kv_tokens(s, layer, c - 1, c)
             ks.append(k)

@@ -86,7 +86,7 @@ def workload_kv(wl, layer: int, device, seqs=None, upto_offset: int = 0):
     spans, slots = [], []
     for s in chosen:
         n = int(wl.context_lens[s]) - upto_offset
-        if n <= 0:
+        if n <= 0 or not wl.has_pages(s):
             continue
         spans.append((s, n))
         slots.append(wl.slot_mapping(s, layer, 0, n))
