@@ -47,7 +47,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny", "trace"], default="bandwidth")
+    p.add_argument("--config", choices=["bandwidth", "llama_step", "ragged", "tiny", "trace", "prefill"],
+                   default="bandwidth")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--ctas", type=int, default=0, help="CTAs of the split-context pass (0 = the library's choice)")
@@ -658,12 +659,119 @@ def run_trace(args):
 
 
 
+# ---------------------------------------------------------------------------
+def run_prefill(args):
+    """Paged prefill: 16 sequences x 512-token prompts (the pages' longest prompt), 1 layer.
+    A step appends every prompt token (kv_append) and runs causal paged prefill attention.
+    Tensor-bound: the roofline counts the causal flops, 4 * head_dim * q_heads * sum_i (p_i + 1)
+    (QK^T and PV, 2 flops per multiply-add), against the measured bf16 tensor peak."""
+    import torch
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import configs, torch_gen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nseq, plen = 16, 512
+    wl = configs.custom(187, [plen] * nseq, name="prefill")
+    steps = args.steps if args.steps is not None else 500
+    warmup = args.warmup if args.warmup is not None else 10
+    pool = pkv.KVPool(wl.num_pages, device=dev)
+    k, v, slots = torch_gen.workload_kv(wl, 0, dev)
+    n = wl.num_seqs * wl.num_q_heads * wl.head_dim * plen
+    q = torch_gen.normal_bf16(rng_key("prefill-q"), 0, n, dev).view(nseq * plen, 32, 64)
+    qs = torch.arange(0, (nseq + 1) * plen, plen, dtype=torch.int32, device=dev)
+    bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables[:, 0, :])).to(dev)
+    lens = torch.from_numpy(wl.context_lens).to(dev)
+    out = torch.empty(nseq * plen, 32, 64, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def attend():
+        pkv.paged_prefill_attention(pool, out, q, qs, bt, bt.shape[1], lens, plen, wl.max_context, wl.scale, status)
+
+    for _ in range(warmup):
+        pkv.kv_append(pool, k, v, slots, status)
+        attend()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    tw0 = time.time()
+    for e in ev:
+        flush_w.zero_()
+        flush_r.max()
+        e[0].record(stream)
+        pkv.kv_append(pool, k, v, slots, status)
+        e[1].record(stream)
+        attend()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    att_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = max_over_ranks(sum(a + b for a, b in zip(app_ms, att_ms)) / steps, dev)
+    flops = 4 * 64 * 32 * nseq * (plen * (plen + 1) // 2)
+    att_s = sum(att_ms) / steps * 1e-3
+    tflops = flops / att_s / 1e12
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    if rank == 0:
+        line = {"metric": "paged prefill attention TFLOP/s (causal) and % of the bf16 tensor peak",
+                "value": round(world * flops / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": steps, "warmup": warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/out",
+                "data": "synthetic (seeded N(0,1) bf16)",
+                "config": {"workload": "prefill", "num_seqs": nseq, "prompt_tokens": plen, "layers": 1,
+                           "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
+                           "l2": "L2 flushed between steps (write of a 2x L2 buffer, then read of another)"},
+                "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tflops / peak, 4), "traffic": None,
+                             "kernel": "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)",
+                             "algorithmic_flops_per_launch": flops,
+                             "avg_launch_us": round(att_s * 1e6, 3),
+                             "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json, cuBLAS burst)"},
+                "kernel_us": {"kv_append (all prompt tokens)": round(1e3 * sum(app_ms) / steps, 3),
+                              "paged_prefill_attention": round(att_s * 1e6, 3)},
+                "clocks": sampler.summary(tw0, tw1), "gpu_launches": 2 * steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def rng_key(tag: str) -> int:
+    from workloads import rng
+    return rng.stream_key(187, tag)
+
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":
         return run_trace(args)
+    if args.config == "prefill":
+        return run_prefill(args)
     return run_native(args)
 
 

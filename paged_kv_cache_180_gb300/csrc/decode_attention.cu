@@ -20,7 +20,7 @@
 //    [c*T/Gu, (c+1)*T/Gu), so every CTA streams the same number of bytes
 //    whatever the mix of context lengths.  Equal-length batches are split along
 //    sequence boundaries instead (a cut costs a merge), and no CTA gets fewer
-//    than 8 pages unless the caller fixes the count.  A sequence
+//    than 4 pages unless the caller fixes the count.  A sequence
 //    covered by one CTA is written out directly; a sequence cut across CTAs
 //    leaves one partial state (m, l, acc) per CTA in the workspace, and for each
 //    group of 4 query heads the last warp to finish (an atomic ticket on a
@@ -72,7 +72,7 @@ constexpr int kWarps = kKvHeads;          // one warp per K/V head
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kCtasPerSm = 2;
-constexpr int kMinPagesPerCta = 8;  // least pages a CTA is given (unless the caller fixes the split)
+constexpr int kMinPagesPerCta = 4;  // least pages a CTA is given (unless the caller fixes the split)
 constexpr int kHeadRowsBytes = kPageTokens * kRowBytes;  // one head's K (or V) rows of a page: 2 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
   // a query row past n is padding: it attends like the last real row and is not written
   const int pos_a = base_pos + min(tok_a, n - 1), pos_b = base_pos + min(tok_b, n - 1);
   const int warp_last_pos = base_pos + min(tw + 15, n - 1);
+  const int warp_first_pos = base_pos + min(tw, n - 1);
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t krow = uint32_t((((mi >> 1) << 3) + ri) * kRowBytes);
   const uint32_t kchunk = uint32_t(mi & 1);
@@ -182,16 +183,27 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
         mma_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
         mma_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
       }
-      // scores in log2 units; key t counts for a row at position p when t <= p (p < ctx)
+      // scores in log2 units; key t counts for a row at position p when t <= p (p < ctx).
+      // Pages wholly at or before every row's position need no mask.
       float xa[4], xb[4];
+      if (key0 + kPageTokens - 1 <= warp_first_pos) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int t = key0 + 8 * nt + 2 * quad + j;
-          xa[2 * nt + j] = (t <= pos_a) ? sc[nt][j] * a.scale_log2 : -INFINITY;
-          xb[2 * nt + j] = (t <= pos_b) ? sc[nt][2 + j] * a.scale_log2 : -INFINITY;
-        }
+          for (int j = 0; j < 2; ++j) {
+            xa[2 * nt + j] = sc[nt][j] * a.scale_log2;
+            xb[2 * nt + j] = sc[nt][2 + j] * a.scale_log2;
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int t = key0 + 8 * nt + 2 * quad + j;
+            xa[2 * nt + j] = (t <= pos_a) ? sc[nt][j] * a.scale_log2 : -INFINITY;
+            xb[2 * nt + j] = (t <= pos_b) ? sc[nt][2 + j] * a.scale_log2 : -INFINITY;
+          }
+      }
       float mxa = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
       float mxb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
       mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
@@ -212,12 +224,14 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
       l_b = l_b * alpha_b + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
       m_a = na;
       m_b = nb;
+      if (!__all_sync(0xffffffffu, alpha_a == 1.f && alpha_b == 1.f)) {  // no row's maximum moved: skip
 #pragma unroll
-      for (int nd = 0; nd < 8; ++nd) {
-        o[nd][0] *= alpha_a;
-        o[nd][1] *= alpha_a;
-        o[nd][2] *= alpha_b;
-        o[nd][3] *= alpha_b;
+        for (int nd = 0; nd < 8; ++nd) {
+          o[nd][0] *= alpha_a;
+          o[nd][1] *= alpha_a;
+          o[nd][2] *= alpha_b;
+          o[nd][3] *= alpha_b;
+        }
       }
       // P as A fragments (rows r, r + 8; keys 2 quad (+1) and 8 + 2 quad (+1)), hi and lo parts
       const uint32_t h0 = pack_bf16x2(pa[0], pa[1]), h1 = pack_bf16x2(pb[0], pb[1]);
