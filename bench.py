@@ -743,7 +743,7 @@ def run_prefill(args):
                            "l2": "L2 flushed between steps (write of a 2x L2 buffer, then read of another)"},
                 "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                              "frac": round(tflops / peak, 4), "traffic": None,
-                             "kernel": "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)",
+                             "kernel": "paged_prefill_kernel (tcgen05.mma M128 N64, TMEM accumulators, P as bf16 hi + lo)",
                              "algorithmic_flops_per_launch": flops,
                              "avg_launch_us": round(att_s * 1e6, 3),
                              "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json, cuBLAS burst)"},

@@ -202,7 +202,8 @@ int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, 
  *   n_s = query_start[s+1] - query_start[s]: the queries are the last n_s cached tokens
  *   (append them with pkv_kv_append first).
  *
- *   out            device; float32 [total][num_q_heads][head_dim], total = query_start[num_seqs].
+ *   out            device; float32 [total][num_q_heads][head_dim], total = query_start[num_seqs],
+ *                  16-byte aligned.
  *   q              device; bf16 [total][num_q_heads][head_dim], 16-byte aligned.
  *   query_start    device; int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
  *   block_tables, block_table_stride, context_lens, max_context: as for decode.

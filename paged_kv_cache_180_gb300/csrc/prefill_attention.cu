@@ -11,23 +11,35 @@
 //   out[i][h] = sum_{t <= p_i} softmax_t(scale * q[i][h] . K_t[h/4]) V_t[h/4],
 //   p_i = context_lens[s] - n_s + (i - query_start[s])
 //
-// GB300 design
-//  * Grid: one CTA per (32-query tile of a sequence, K/V head g).  Warp w serves
-//    query head 4g + (w % 4) for 16 query tokens (w / 4 picks which 16), so the
-//    8 warps share every K/V row the CTA loads.  Tiles are numbered latest-first
-//    within a sequence so the longest causal spans start first.
-//  * Staging: head g's 16 rows of each page arrive as two tiled TMA boxes
-//    (2 KiB of K, 2 KiB of V, 128-byte swizzle) into a ring of stages with
-//    mbarriers; the last warp done with a stage refills it (no producer warp).
-//  * Math on the tensor cores: S[16 tokens x 16 keys] = Q K^T as 2 x 4
-//    mma.sync m16n8k16 (bf16 in, fp32 accumulate; K by ldmatrix), online softmax
-//    per row on the accumulator fragments (exp2 domain, quad shuffles), and
-//    O += P V with P split into bf16 hi + lo parts (two MMAs per 8-dim tile; V by
-//    ldmatrix.trans) so the weights keep ~16 significant bits.
-//  * Masks: key t counts for query i when t <= p_i; keys at or past the context
-//    get -inf and zeroed V fragments, so stale pool bytes never reach the sums.
-//    A warp skips pages that lie wholly after its last query's position.
-//  * Every mbarrier wait is bounded (about 2 s) and reports PKV_DEV_TIMEOUT.
+// GB300 design (tcgen05 tensor cores, accumulators in tensor memory)
+//  * Tile: one CTA per (32 query tokens of a sequence, K/V head g).  Its 128 rows
+//    (row = 4 * token + head in group) share every K/V row it loads: M = 128.
+//    Tiles are numbered latest-first over the whole grid, so the longest causal
+//    spans start first.
+//  * Keys in blocks of 64 (4 pages).  S = Q K^T is 4 tcgen05.mma (M 128, N 64,
+//    K 16 each; Q and K K-major, 128-byte swizzled) into one of two TMEM
+//    buffers, so S of block j + 1 runs while the softmax reads block j.
+//    O += P V is 8 tcgen05.mma into a TMEM accumulator: P is split into bf16
+//    hi + lo halves (weights keep ~16 significant bits), both multiplied by the
+//    same V tile (MN-major, 128-byte swizzled).
+//  * Warp roles: warps 0-3 own one row each per thread (TMEM lane = row): they
+//    load Q, read S from TMEM, mask, keep the row's running max and sum, write P
+//    to shared memory and finally read O, divide and store.  Warp 4 streams head
+//    g's K and V rows of each page with tiled TMA (2 KiB boxes) into a 3-stage
+//    ring; pages past the query span are loaded from a coordinate outside the
+//    pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and
+//    issues the MMAs (one thread), completion signalled by tcgen05.commit.
+//  * Online softmax in the exp2 domain with a lazily moved maximum: a row's
+//    reference maximum moves only when a block's maximum exceeds it by more than
+//    8 (a factor 256), and only then is the row of O in TMEM rescaled (after the
+//    previous P V completed).  The final division by the row sum uses the same
+//    reference, so the result is the exact softmax up to rounding.
+//  * Masks: key t counts for a row at position p when t <= p (p < ctx); other
+//    scores become -inf.  V rows at or past the context in a sequence's last page
+//    are zeroed in shared memory so stale pool bytes (even NaN) never reach O.
+//  * Every mbarrier wait is bounded (about 2 s): on expiry the CTA reports
+//    PKV_DEV_TIMEOUT, stops issuing work, waits (bounded) for what is in flight,
+//    frees its tensor memory and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,19 +52,29 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfStages = 4;
-constexpr int kPfWarps = 8;
-constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kPfTile = 32;                          // query tokens per CTA (2 x 16)
-constexpr int kBox = kPageTokens * kRowBytes;        // one head's rows of one page: 2 KiB
+constexpr int kPfTok = 32;                             // query tokens per CTA
+constexpr int kPfRows = kPfTok * kGroup;               // M = 128
+constexpr int kPfKeys = 64;                            // keys per block
+constexpr int kPfPagesPerBlock = kPfKeys / kPageTokens;
+constexpr int kPfStages = 3;
+constexpr int kPfThreads = 192;                        // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kPfBox = kPageTokens * kRowBytes;        // one head's rows of one page: 2 KiB
+constexpr int kPfTileBytes = kPfKeys * kRowBytes;      // K (or V) of one block: 8 KiB
+constexpr uint32_t kPfTmemCols = 256;
+constexpr uint32_t kColS = 0;                          // S buffers at columns 0 and 64
+constexpr uint32_t kColO = 128;                        // O accumulator: columns 128 .. 191
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.f;                    // move a row's reference max when exceeded by more
+
+constexpr uint32_t kIdescS = idesc_bf16(kPfRows, kPfKeys, false);   // B = K rows (K-major)
+constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, kHeadDim, true);  // B = V rows (MN-major)
 
 struct PrefillArgs {
   CUtensorMap tmap_k;  // boxes of one head's 16 rows of one page
   CUtensorMap tmap_v;
   int num_pages;
-  const uint32_t *q;  // [total][32][64] bf16 as pairs
-  float *out;         // [total][32][64]
+  const uint4 *q;  // [total][32][64] bf16, 8 uint4 per head row
+  float *out;      // [total][32][64]
   const int32_t *query_start;
   const int32_t *block_tables;
   long long bt_stride;
@@ -65,236 +87,332 @@ struct PrefillArgs {
 };
 
 struct __align__(1024) PfSmem {
-  uint8_t kv[kPfStages][2][kBox];  // [stage][K|V], 2 KiB each (1024-byte aligned)
-  uint64_t full[kPfStages];
-  int stage_ok[kPfStages];
-  unsigned stage_done[kPfStages];
-  unsigned long long issued;
-  int any_aborted;
+  uint8_t q[kPfRows * kRowBytes];          // 16 KiB, row = 4 * token + head, 128-byte swizzled
+  uint8_t k[kPfStages][kPfTileBytes];      // 64 keys x 128 B per stage
+  uint8_t v[kPfStages][kPfTileBytes];
+  uint8_t p_hi[kPfRows * kRowBytes];       // P of the current block: 128 rows x 64 keys bf16
+  uint8_t p_lo[kPfRows * kRowBytes];
+  uint64_t q_full;
+  uint64_t kv_full[kPfStages];
+  uint64_t kv_empty[kPfStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t p_free;  // P V of a block done (P buffer and O free)
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
 };
 constexpr size_t kPfSmemBytes = sizeof(PfSmem) + 1024;
 
-__device__ __forceinline__ void pf_issue(const PrefillArgs &a, PfSmem &sm, int st, int page, int g, uint64_t policy) {
-  if (page >= 0 && page < a.num_pages) {
-    sm.stage_ok[st] = 1;
-    mbar_arrive_expect_tx(&sm.full[st], 2 * kBox);
-    tma_load_3d(sm.kv[st][0], &a.tmap_k, 0, g * kPageTokens, page, &sm.full[st], policy);
-    tma_load_3d(sm.kv[st][1], &a.tmap_v, 0, g * kPageTokens, page, &sm.full[st], policy);
-  } else {
-    report(a.status, PKV_DEV_BAD_PAGE);
-    sm.stage_ok[st] = 0;
-    mbar_arrive(&sm.full[st]);
-  }
+// Bounded wait that gives up at once when another role has already aborted.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool pf_wait(PfSmem &sm, uint64_t *bar, uint32_t parity, int32_t *status) {
+  if (*reinterpret_cast<volatile int *>(&sm.abort)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *reinterpret_cast<volatile int *>(&sm.abort) = 1;
+  report(status, PKV_DEV_TIMEOUT);
+  return false;
+}
+
+// Writes 8 16-byte chunks as row r of a 128-byte-swizzled tile.
+__device__ __forceinline__ void put_row_sw128(uint8_t *tile, int r, const uint4 (&c)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4 *>(tile + r * kRowBytes + ((i ^ (r & 7)) << 4)) = c[i];
 }
 
 __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   PfSmem &sm = *reinterpret_cast<PfSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.x / a.tiles_per_seq;
-  const int tile = a.tiles_per_seq - 1 - int(blockIdx.x % a.tiles_per_seq);
-  const int g = blockIdx.y;
+  // tile rank r (latest tiles first over the grid), then sequence, then K/V head
+  const int per_rank = a.num_seqs * kKvHeads;
+  const int rank = int(blockIdx.x) / per_rank, rem = int(blockIdx.x) % per_rank;
+  const int s = rem / kKvHeads, g = rem % kKvHeads;
+  const int tile = a.tiles_per_seq - 1 - rank;
   const int q0 = __ldg(a.query_start + s);
   const int n = __ldg(a.query_start + s + 1) - q0;
   const int ctx = __ldg(a.context_lens + s);
-  const int t0 = tile * kPfTile;
+  const int t0 = tile * kPfTok;
   if (n <= 0 || t0 >= n) return;
-  const int tend = min(t0 + kPfTile, n);
+  const int tend = min(t0 + kPfTok, n);
   if (ctx < 0 || ctx > a.max_context || n > ctx) {
     // invalid sequence: zero this CTA's rows (its tokens, query heads 4g .. 4g+3)
     if (tile == 0 && g == 0 && tid == 0) report(a.status, PKV_DEV_BAD_CONTEXT);
     for (int k = tid; k < (tend - t0) * kGroup * kHeadDim; k += kPfThreads) {
-      const int tok = t0 + k / (kGroup * kHeadDim), rem = k % (kGroup * kHeadDim);
-      a.out[((long long)(q0 + tok) * kQHeads + g * kGroup) * kHeadDim + rem] = 0.f;
+      const int tok = t0 + k / (kGroup * kHeadDim), r = k % (kGroup * kHeadDim);
+      a.out[((long long)(q0 + tok) * kQHeads + g * kGroup) * kHeadDim + r] = 0.f;
     }
     return;
   }
-  const int base_pos = ctx - n;                      // position of query token 0
-  const int npages = (base_pos + tend - 1) / kPageTokens + 1;
+  const int base_pos = ctx - n;                         // position of query token 0
+  const int last_pos = base_pos + tend - 1;             // latest position in this tile
+  const int nblocks = last_pos / kPfKeys + 1;
+  const int npages = last_pos / kPageTokens + 1;        // pages holding keys 0 .. last_pos
   const int32_t *table = a.block_tables + (long long)s * a.bt_stride;
 
   if (tid == 0) {
+    mbar_init(&sm.q_full, 128);
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&sm.full[i], 1);
-      sm.stage_done[i] = 0;
+      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
     }
-    sm.issued = 0;
-    sm.any_aborted = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.s_free[b], 128);
+    }
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.p_free, 1);
+    mbar_init(&sm.mma_done, 1);
+    sm.abort = 0;
     mbar_init_fence();
   }
+  if (warp == 5) tmem_alloc(&sm.tmem_base, kPfTmemCols);
+  tc_fence_before();
   __syncthreads();
-  const uint64_t policy = policy_evict_first();
-  if (tid == 0) {
-    prefetch_tensormap(&a.tmap_k);
-    prefetch_tensormap(&a.tmap_v);
-    const int first = npages < kPfStages ? npages : kPfStages;
-    for (int j = 0; j < first; ++j) pf_issue(a, sm, j, __ldg(table + j), g, policy);
-    atomicMax(&sm.issued, (unsigned long long)first);
-  }
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
 
-  // ---- this warp: query head hq, tokens tw .. tw+15 (rows r = lane/4 and r + 8) ----
-  const int hq = g * kGroup + (warp & 3);
-  const int tw = t0 + 16 * (warp >> 2);
-  const int quad = lane & 3, r = lane >> 2;
-  const int tok_a = tw + r, tok_b = tw + r + 8;      // query tokens of fragment rows r and r + 8
-  // a query row past n is padding: it attends like the last real row and is not written
-  const int pos_a = base_pos + min(tok_a, n - 1), pos_b = base_pos + min(tok_b, n - 1);
-  const int warp_last_pos = base_pos + min(tw + 15, n - 1);
-  const int warp_first_pos = base_pos + min(tw, n - 1);
-  const int mi = lane >> 3, ri = lane & 7;
-  const uint32_t krow = uint32_t((((mi >> 1) << 3) + ri) * kRowBytes);
-  const uint32_t kchunk = uint32_t(mi & 1);
-  const uint32_t vrow = uint32_t((((mi & 1) << 3) + ri) * kRowBytes);
-  const uint32_t vchunk = uint32_t(mi >> 1);
-  uint32_t qa[4][4];  // A fragments per k-step: rows r, r+8; k pairs 2 quad and 8 + 2 quad
-  {
-    const bool va = tw < n && tok_a < n, vb = tok_b < n;
-    const uint32_t *ra = a.q + ((long long)(q0 + min(tok_a, n - 1)) * kQHeads + hq) * (kHeadDim / 2);
-    const uint32_t *rb = a.q + ((long long)(q0 + min(tok_b, n - 1)) * kQHeads + hq) * (kHeadDim / 2);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[ks][0] = va ? __ldg(ra + ks * 8 + quad) : 0u;
-      qa[ks][1] = vb ? __ldg(rb + ks * 8 + quad) : 0u;
-      qa[ks][2] = va ? __ldg(ra + ks * 8 + 4 + quad) : 0u;
-      qa[ks][3] = vb ? __ldg(rb + ks * 8 + 4 + quad) : 0u;
-    }
-  }
-  float o[8][4];
-#pragma unroll
-  for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  bool aborted = false;
-
-  for (int pg = 0; pg < npages; ++pg) {
-    const int st = pg % kPfStages;
-    if (!aborted && !mbar_wait(&sm.full[st], uint32_t(pg / kPfStages) & 1)) {
-      report(a.status, PKV_DEV_TIMEOUT);
-      aborted = true;
-    }
-    const int key0 = pg * kPageTokens;
-    if (!aborted && sm.stage_ok[st] && key0 <= warp_last_pos) {
-      const uint32_t kbase = smem_addr(sm.kv[st][0]);
-      const uint32_t vbase = smem_addr(sm.kv[st][1]);
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t b00, b01, b10, b11;
-        ldmatrix_x4(kbase + krow + (((2 * ks + kchunk) ^ ri) << 4), b00, b01, b10, b11);
-        mma_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-        mma_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
-      }
-      // scores in log2 units; key t counts for a row at position p when t <= p (p < ctx).
-      // Pages wholly at or before every row's position need no mask.
-      float xa[4], xb[4];
-      if (key0 + kPageTokens - 1 <= warp_first_pos) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            xa[2 * nt + j] = sc[nt][j] * a.scale_log2;
-            xb[2 * nt + j] = sc[nt][2 + j] * a.scale_log2;
+  if (warp == 4) {
+    // ================= TMA producer: head g's K and V rows, 4 pages per block =================
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_last();
+      prefetch_tensormap(&a.tmap_k);
+      prefetch_tensormap(&a.tmap_v);
+      int issued = 0;
+      for (int j = 0; j < nblocks; ++j) {
+        const int st = j % kPfStages;
+        if (j >= kPfStages && !pf_wait(sm, &sm.kv_empty[st], uint32_t(j / kPfStages - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kPfTileBytes);
+        for (int pp = 0; pp < kPfPagesPerBlock; ++pp) {
+          const int lp = j * kPfPagesPerBlock + pp;
+          int page = -1;  // outside the pool: TMA fills the box with zeros
+          if (lp < npages) {
+            page = __ldg(table + lp);
+            if (page < 0 || page >= a.num_pages) {
+              report(a.status, PKV_DEV_BAD_PAGE);
+              page = -1;
+            }
           }
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int t = key0 + 8 * nt + 2 * quad + j;
-            xa[2 * nt + j] = (t <= pos_a) ? sc[nt][j] * a.scale_log2 : -INFINITY;
-            xb[2 * nt + j] = (t <= pos_b) ? sc[nt][2 + j] * a.scale_log2 : -INFINITY;
-          }
+          tma_load_3d(sm.k[st] + pp * kPfBox, &a.tmap_k, 0, g * kPageTokens, page, &sm.kv_full[st], policy);
+          tma_load_3d(sm.v[st] + pp * kPfBox, &a.tmap_v, 0, g * kPageTokens, page, &sm.kv_full[st], policy);
+        }
+        issued = j + 1;
       }
-      float mxa = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
-      float mxb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
-      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-      // a row whose keys here are all masked keeps its state (its max stays as it was)
-      const float na = fmaxf(m_a, mxa), nb = fmaxf(m_b, mxb);
-      const float alpha_a = (na == -INFINITY) ? 1.f : exp2f(m_a - na);
-      const float alpha_b = (nb == -INFINITY) ? 1.f : exp2f(m_b - nb);
-      float pa[4], pb[4];
+      // every copy issued has landed before the CTA exits
+      for (int j = max(0, issued - kPfStages); j < issued; ++j)
+        mbar_wait(&sm.kv_full[j % kPfStages], uint32_t(j / kPfStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ================= MMA issuer =================
+    const uint32_t q_base = smem_addr(sm.q), phi = smem_addr(sm.p_hi), plo = smem_addr(sm.p_lo);
+    bool ok = pf_wait(sm, &sm.q_full, 0, a.status);
+    ok = __all_sync(0xffffffffu, ok);
+    auto issue_pv = [&](int i) {
+      bool w = pf_wait(sm, &sm.p_full, uint32_t(i) & 1, a.status);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const int st = i % kPfStages;
+        const uint32_t vb = smem_addr(sm.v[st]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pa[k] = (na == -INFINITY) ? 0.f : exp2f(xa[k] - na);
-        pb[k] = (nb == -INFINITY) ? 0.f : exp2f(xb[k] - nb);
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tmem + kColO, sw128_desc(phi + kk * 32, 16, 1024), sw128_desc(vb + kk * 2048, 1024, 1024), kIdescPV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tmem + kColO, sw128_desc(plo + kk * 32, 16, 1024), sw128_desc(vb + kk * 2048, 1024, 1024), kIdescPV,
+                 1u);
+        tc_commit(&sm.p_free);
+        tc_commit(&sm.kv_empty[st]);
       }
-      l_a = l_a * alpha_a + ((pa[0] + pa[1]) + (pa[2] + pa[3]));
-      l_b = l_b * alpha_b + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
-      m_a = na;
-      m_b = nb;
-      if (!__all_sync(0xffffffffu, alpha_a == 1.f && alpha_b == 1.f)) {  // no row's maximum moved: skip
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; ok && j < nblocks; ++j) {
+      const int st = j % kPfStages, b = j & 1;
+      bool w = pf_wait(sm, &sm.kv_full[st], uint32_t(j / kPfStages) & 1, a.status);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) break;
+      // V rows at or past the context (stale pool bytes) in this block become zeros
+      const int z0 = max(ctx, j * kPfKeys), z1 = min(npages * kPageTokens, (j + 1) * kPfKeys);
+      if (z0 < z1) {
+        uint8_t *vt = sm.v[st];
+        for (int idx = lane; idx < (z1 - z0) * 8; idx += 32)
+          *reinterpret_cast<uint4 *>(vt + (z0 - j * kPfKeys + idx / 8) * kRowBytes + (idx % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (j >= 2) {
+        w = pf_wait(sm, &sm.s_free[b], uint32_t(j / 2 - 1) & 1, a.status);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kb = smem_addr(sm.k[st]);
 #pragma unroll
-        for (int nd = 0; nd < 8; ++nd) {
-          o[nd][0] *= alpha_a;
-          o[nd][1] *= alpha_a;
-          o[nd][2] *= alpha_b;
-          o[nd][3] *= alpha_b;
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tmem + kColS + b * kPfKeys, sw128_desc(q_base + kk * 32, 16, 1024), sw128_desc(kb + kk * 32, 16, 1024),
+                 kIdescS, kk > 0 ? 1u : 0u);
+        tc_commit(&sm.s_full[b]);
+      }
+      __syncwarp();
+      if (j >= 1 && !issue_pv(j - 1)) {
+        ok = false;
+        break;
+      }
+      if (j == nblocks - 1 && !issue_pv(j)) ok = false;
+    }
+    // every MMA issued has completed before the tensor memory is freed
+    if (lane == 0) {
+      tc_commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax warps: thread = row = 4 * token + head =================
+    const int r = tid, tok = r >> 2, hh = r & 3;
+    {
+      // Q row (a padding row past n repeats the last real token; it is not written)
+      const uint4 *src = a.q + ((long long)(q0 + min(t0 + tok, n - 1)) * kQHeads + g * kGroup + hh) * 8;
+      uint4 c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = __ldg(src + i);
+      put_row_sw128(sm.q, r, c);
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.q_full);
+    }
+    const int pos = base_pos + min(t0 + tok, n - 1);
+    const uint32_t lane_base = tmem + (uint32_t(32 * warp) << 16);
+    float m_ref = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nblocks; ++j) {
+      const int b = j & 1;
+      bool w = pf_wait(sm, &sm.s_full[b], uint32_t(j >> 1) & 1, a.status);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[64];
+      {
+        uint32_t x0[32], x1[32];
+        tmem_ld32(lane_base + kColS + b * kPfKeys, x0);
+        tmem_ld32(lane_base + kColS + b * kPfKeys + 32, x1);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = x0[c];
+          sv[32 + c] = x1[c];
         }
       }
-      // P as A fragments (rows r, r + 8; keys 2 quad (+1) and 8 + 2 quad (+1)), hi and lo parts
-      const uint32_t h0 = pack_bf16x2(pa[0], pa[1]), h1 = pack_bf16x2(pb[0], pb[1]);
-      const uint32_t h2 = pack_bf16x2(pa[2], pa[3]), h3 = pack_bf16x2(pb[2], pb[3]);
-      const uint32_t l0 = pack_bf16x2(pa[0] - bf16_lo(h0), pa[1] - bf16_hi(h0));
-      const uint32_t l1 = pack_bf16x2(pb[0] - bf16_lo(h1), pb[1] - bf16_hi(h1));
-      const uint32_t l2 = pack_bf16x2(pa[2] - bf16_lo(h2), pa[3] - bf16_hi(h2));
-      const uint32_t l3 = pack_bf16x2(pb[2] - bf16_lo(h3), pb[3] - bf16_hi(h3));
-      // V fragments hold keys 2 quad (+1) and 8 + 2 quad (+1): zero those at or past the context
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (key0 + kPageTokens > ctx) {
-        const int k0 = key0 + 2 * quad;
-        vm_lo = (k0 < ctx ? 0x0000ffffu : 0u) | (k0 + 1 < ctx ? 0xffff0000u : 0u);
-        vm_hi = (k0 + 8 < ctx ? 0x0000ffffu : 0u) | (k0 + 9 < ctx ? 0xffff0000u : 0u);
-      }
+      tc_fence_before();
+      mbar_arrive(&sm.s_free[b]);
+      // scores in log2 units; keys after this row's position, and the keys of
+      // invalid pages (loaded as zeros), are masked
+      const int key0 = j * kPfKeys;
+      int bad = 0;
 #pragma unroll
-      for (int nd = 0; nd < 8; nd += 2) {
-        uint32_t v0, v1, v2, v3;
-        ldmatrix_x4_trans(vbase + vrow + (((nd + vchunk) ^ ri) << 4), v0, v1, v2, v3);
-        v0 &= vm_lo;
-        v1 &= vm_hi;
-        v2 &= vm_lo;
-        v3 &= vm_hi;
-        mma_16816(o[nd], h0, h1, h2, h3, v0, v1);
-        mma_16816(o[nd], l0, l1, l2, l3, v0, v1);
-        mma_16816(o[nd + 1], h0, h1, h2, h3, v2, v3);
-        mma_16816(o[nd + 1], l0, l1, l2, l3, v2, v3);
+      for (int pp = 0; pp < kPfPagesPerBlock; ++pp) {
+        const int lp = j * kPfPagesPerBlock + pp;
+        if (lp < npages) {
+          const int page = __ldg(table + lp);
+          if (page < 0 || page >= a.num_pages) bad |= 1 << pp;
+        }
+      }
+      float x[64];
+      float mx = -INFINITY;
+      if (key0 + kPfKeys - 1 <= pos && bad == 0) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          x[c] = __uint_as_float(sv[c]) * a.scale_log2;
+          mx = fmaxf(mx, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          x[c] = (key0 + c <= pos && !((bad >> (c / kPageTokens)) & 1)) ? __uint_as_float(sv[c]) * a.scale_log2
+                                                                          : -INFINITY;
+          mx = fmaxf(mx, x[c]);
+        }
+      }
+      // move the reference max only when this block's max exceeds it by more than 2^8
+      const bool move = mx > m_ref + kRescaleLog2;
+      float alpha = 1.f;
+      if (move) {
+        alpha = exp2f(m_ref - mx);  // 0 for the first block (m_ref = -inf)
+        m_ref = mx;
+        l_sum *= alpha;
+      }
+      float psum = 0.f;
+      uint4 hi[8], lo[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t h4[4], l4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = exp2f(x[8 * c + 2 * e] - m_ref), p1 = exp2f(x[8 * c + 2 * e + 1] - m_ref);
+          psum += p0 + p1;
+          h4[e] = pack_bf16x2(p0, p1);
+          l4[e] = pack_bf16x2(p0 - bf16_lo(h4[e]), p1 - bf16_hi(h4[e]));
+        }
+        hi[c] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        lo[c] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+      }
+      l_sum += psum;
+      if (j >= 1) {
+        // P V of the previous block has finished: P may be overwritten and O rescaled
+        w = pf_wait(sm, &sm.p_free, uint32_t(j - 1) & 1, a.status);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + 32 * half, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(lane_base + kColO + 32 * half, o);
+          }
+        }
+      }
+      put_row_sw128(sm.p_hi, r, hi);
+      put_row_sw128(sm.p_lo, r, lo);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full);
+    }
+    // ---- epilogue: O / l for the rows of real query tokens ----
+    bool w = ok && pf_wait(sm, &sm.p_free, uint32_t(nblocks - 1) & 1, a.status);
+    if (__all_sync(0xffffffffu, w)) {
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      float *dst = a.out + ((long long)(q0 + t0 + tok) * kQHeads + g * kGroup + hh) * kHeadDim;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + 32 * half, o);
+        if (t0 + tok < n) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4 *>(dst + 32 * half + c) =
+                make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                            __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+        }
       }
     }
-    // the last warp done with this stage refills it with the page kPfStages ahead
-    __syncwarp();
-    if (pg + kPfStages < npages && lane == 0 && !aborted) {
-      const unsigned done = atomicAdd(&sm.stage_done[st], 1u) + 1u;
-      if (done % kPfWarps == 0) {
-        pf_issue(a, sm, st, __ldg(table + pg + kPfStages), g, policy);
-        atomicMax(&sm.issued, (unsigned long long)(pg + kPfStages + 1));
-      }
-    }
-    if (aborted && lane == 0) sm.any_aborted = 1;
   }
-
-  // ---- write the rows of real query tokens ----
-  float la = l_a + __shfl_xor_sync(0xffffffffu, l_a, 1);
-  la += __shfl_xor_sync(0xffffffffu, la, 2);
-  float lb = l_b + __shfl_xor_sync(0xffffffffu, l_b, 1);
-  lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-  const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
-  if (tok_a < n) {
-    float *dst = a.out + ((long long)(q0 + tok_a) * kQHeads + hq) * kHeadDim + 2 * quad;
-#pragma unroll
-    for (int nd = 0; nd < 8; ++nd) *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] * ia, o[nd][1] * ia);
-  }
-  if (tok_b < n) {
-    float *dst = a.out + ((long long)(q0 + tok_b) * kQHeads + hq) * kHeadDim + 2 * quad;
-#pragma unroll
-    for (int nd = 0; nd < 8; ++nd) *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][2] * ib, o[nd][3] * ib);
-  }
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0 && sm.any_aborted) {
-    const long long issued = (long long)sm.issued;
-    const long long first = issued > kPfStages ? issued - kPfStages : 0;
-    for (long long j = first; j < issued; ++j)
-      mbar_wait(&sm.full[int(j % kPfStages)], uint32_t(j / kPfStages) & 1);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPfTmemCols);
   }
 }
 
@@ -323,19 +441,18 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   if (out == nullptr || q == nullptr || query_start == nullptr || block_tables == nullptr || context_lens == nullptr)
     return PKV_ERR_NULL;
   if (!isfinite(scale)) return PKV_ERR_SCALE;
-  if (!pkv::aligned16(q) || (reinterpret_cast<uintptr_t>(out) & 7u) ||
-      (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
-      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+  if (!pkv::aligned16(q) || !pkv::aligned16(out) || (reinterpret_cast<uintptr_t>(query_start) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_ALIGN;
-  const long long tiles = (max_query + pkv::kPfTile - 1) / pkv::kPfTile;
-  if ((long long)num_seqs * tiles > 0x7fffffffLL) return PKV_ERR_SHAPE;
+  const long long tiles = (max_query + pkv::kPfTok - 1) / pkv::kPfTok;
+  if ((long long)num_seqs * tiles * pkv::kKvHeads > 0x7fffffffLL) return PKV_ERR_SHAPE;
   rc = pkv::setup_prefill_attributes();
   if (rc != PKV_OK) return rc;
   pkv::PrefillArgs a;
   rc = pkv::pool_tensor_maps(pool, pkv::kPageTokens, &a.tmap_k, &a.tmap_v);
   if (rc != PKV_OK) return rc;
   a.num_pages = pool->num_pages;
-  a.q = static_cast<const uint32_t *>(q);
+  a.q = static_cast<const uint4 *>(q);
   a.out = out;
   a.query_start = query_start;
   a.block_tables = block_tables;
@@ -346,7 +463,7 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   a.tiles_per_seq = int(tiles);
   a.scale_log2 = scale * pkv::kLog2e;
   a.status = device_status;
-  const dim3 grid(unsigned(num_seqs * tiles), unsigned(pkv::kKvHeads));
+  const unsigned grid = unsigned((long long)num_seqs * tiles * pkv::kKvHeads);
   pkv::paged_prefill_kernel<<<grid, pkv::kPfThreads, pkv::kPfSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
