@@ -210,6 +210,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem]: A's row i in lane i, column c holding its K elements
+// 2c (low half) and 2c + 1 (high half); issued by one thread.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The mbarrier receives one arrival once every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -243,6 +254,51 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 #undef PKV_R8
 #undef PKV_S8
+
+// One column of this thread's TMEM lane, waited for.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+               : "=r"(v)
+               : "r"(taddr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+               "r"(v)
+               : "memory");
+}
+
+// ---- packed fp32 pairs and the hardware base-2 exponential ----
+// (x - m) * c on both halves of a pair, one packed subtract and one packed multiply.
+__device__ __forceinline__ float2 sub_mul_f32x2(float2 x, float2 m, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 xa, ma, ca, d;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 ma, {%4, %5};\n\tmov.b64 ca, {%6, %7};\n\t"
+      "sub.rn.f32x2 d, xa, ma;\n\tmul.rn.f32x2 d, d, ca;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x.x), "f"(x.y), "f"(m.x), "f"(m.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 sub_f32x2(float2 x, float2 y) {
+  float2 r;
+  asm("{\n\t.reg .b64 xa, ya, d;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 ya, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, xa, ya;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return r;
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; subnormal results flush to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 // L2 policy for data several CTAs read in turn (a sequence's K/V in prefill): evict last.
 __device__ __forceinline__ uint64_t policy_evict_last() {

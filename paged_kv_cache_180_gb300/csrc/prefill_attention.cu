@@ -52,22 +52,23 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfTok = 32;                             // query tokens per CTA
+constexpr int kPfTok = 32;                             // query tokens per tile
 constexpr int kPfRows = kPfTok * kGroup;               // M = 128
 constexpr int kPfKeys = 64;                            // keys per block
 constexpr int kPfPagesPerBlock = kPfKeys / kPageTokens;
-constexpr int kPfStages = 3;
-constexpr int kPfThreads = 192;                        // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kPfStages = 4;                           // K/V blocks in flight
+constexpr int kPfThreads = 192;                        // warps 0-3 softmax, 4 loads, 5 MMA
+constexpr int kPfCtasPerSm = 2;
 constexpr int kPfBox = kPageTokens * kRowBytes;        // one head's rows of one page: 2 KiB
 constexpr int kPfTileBytes = kPfKeys * kRowBytes;      // K (or V) of one block: 8 KiB
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kColS = 0;                          // S buffers at columns 0 and 64
-constexpr uint32_t kColO = 128;                        // O accumulator: columns 128 .. 191
+constexpr uint32_t kColO = 128;                        // O: columns 128 .. 191, row sum l at 192, 193 .. 255 zero
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;                    // move a row's reference max when exceeded by more
 
 constexpr uint32_t kIdescS = idesc_bf16(kPfRows, kPfKeys, false);   // B = K rows (K-major)
-constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, kHeadDim, true);  // B = V rows (MN-major)
+constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, 2 * kHeadDim, true);  // B = [V | ones] (MN-major)
 
 struct PrefillArgs {
   CUtensorMap tmap_k;  // boxes of one head's 16 rows of one page
@@ -82,28 +83,61 @@ struct PrefillArgs {
   int num_seqs;
   int max_context;
   int tiles_per_seq;
-  float scale_log2;
+  int num_tiles;  // num_seqs * tiles_per_seq * 8
+  float scale_log2;   // |scale| * log2(e)
+  float move_thresh;  // scores (unscaled) by which a block's max must pass the reference to move it
+  uint32_t q_sign;    // 0x80008000 when scale < 0: Q is negated on load, so the scores use |scale|
   int32_t *status;
 };
 
 struct __align__(1024) PfSmem {
-  uint8_t q[kPfRows * kRowBytes];          // 16 KiB, row = 4 * token + head, 128-byte swizzled
+  uint8_t q[2][kPfRows * kRowBytes];       // two tiles' Q, row = 4 * token + head, 128-byte swizzled
   uint8_t k[kPfStages][kPfTileBytes];      // 64 keys x 128 B per stage
   uint8_t v[kPfStages][kPfTileBytes];
-  uint8_t p_hi[kPfRows * kRowBytes];       // P of the current block: 128 rows x 64 keys bf16
-  uint8_t p_lo[kPfRows * kRowBytes];
-  uint64_t q_full;
+  uint8_t ones[kPfTileBytes];              // the second MN atom of P V's B: 1 in column 0 of every key row
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
   uint64_t kv_full[kPfStages];
   uint64_t kv_empty[kPfStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t p_free;  // P V of a block done (P buffer and O free)
+  uint64_t s_free[2];  // the P V that read a buffer's P is done: S may be written again
+  uint64_t p_full[2];  // per P buffer: every softmax thread wrote its row of P (one barrier per
+                       // buffer, so a thread already on the next block cannot complete this phase)
+  uint64_t p_free[2];  // per P buffer: the P V of a block done (O, and everything before, may be read);
+                       // per buffer so that the phase waited for is never two behind
   uint64_t mma_done;
+  int kv_bad[kPfStages];  // per stage: bit pp set when page pp of the block is invalid (loaded as zeros)
   uint32_t tmem_base;
   int abort;
 };
 constexpr size_t kPfSmemBytes = sizeof(PfSmem) + 1024;
+
+// One work tile: 32 query tokens of sequence s (from t0) against K/V head g.
+struct PfTile {
+  int s, g, t0, n, q0, ctx, nblocks, npages;
+  bool run;      // has queries and a valid context
+  bool invalid;  // has queries, invalid context: its rows are zeroed
+};
+
+// Tile ti of the grid-wide list: latest token tiles first, then sequence, then K/V head.
+__device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int ti) {
+  PfTile t;
+  const int per_rank = a.num_seqs * kKvHeads;
+  const int rank = ti / per_rank, rem = ti % per_rank;
+  t.s = rem / kKvHeads;
+  t.g = rem % kKvHeads;
+  t.t0 = (a.tiles_per_seq - 1 - rank) * kPfTok;
+  t.q0 = __ldg(a.query_start + t.s);
+  t.n = __ldg(a.query_start + t.s + 1) - t.q0;
+  t.ctx = __ldg(a.context_lens + t.s);
+  const bool has = t.n > 0 && t.t0 < t.n;
+  t.invalid = has && (t.ctx < 0 || t.ctx > a.max_context || t.n > t.ctx);
+  t.run = has && !t.invalid;
+  const int last_pos = t.run ? t.ctx - t.n + min(t.t0 + kPfTok, t.n) - 1 : 0;
+  t.nblocks = last_pos / kPfKeys + 1;
+  t.npages = last_pos / kPageTokens + 1;  // pages holding keys 0 .. last_pos
+  return t;
+}
 
 // Bounded wait that gives up at once when another role has already aborted.
 // Returns true when the phase completed.
@@ -115,57 +149,74 @@ __device__ __forceinline__ bool pf_wait(PfSmem &sm, uint64_t *bar, uint32_t pari
   return false;
 }
 
-// Writes 8 16-byte chunks as row r of a 128-byte-swizzled tile.
-__device__ __forceinline__ void put_row_sw128(uint8_t *tile, int r, const uint4 (&c)[8]) {
+// Largest of 64 values (a tree, so the chain is 6 deep).
+__device__ __forceinline__ float max64(const float (&x)[64]) {
+  float m[32];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4 *>(tile + r * kRowBytes + ((i ^ (r & 7)) << 4)) = c[i];
+  for (int c = 0; c < 32; ++c) m[c] = fmaxf(x[c], x[c + 32]);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int c = 0; c < w; ++c) m[c] = fmaxf(m[c], m[c + w]);
+  return m[0];
 }
 
-__global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __grid_constant__ PrefillArgs a) {
+// P = 2^((s - m) * c) for the 64 keys of a block as bf16 hi + lo parts, keys 2i and
+// 2i + 1 packed in word i; with kMasked, keys whose bit in `valid` is clear get 0.
+template <bool kMasked>
+__device__ __forceinline__ void block_probs(const float (&sv)[64], uint64_t valid, float m, float2 c2,
+                                            uint32_t (&hi)[32], uint32_t (&lo)[32]) {
+  const float2 m2 = make_float2(m, m);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float2 e = sub_mul_f32x2(make_float2(sv[2 * i], sv[2 * i + 1]), m2, c2);
+    float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+    if (kMasked) {
+      p0 = (valid >> (2 * i)) & 1 ? p0 : 0.f;
+      p1 = (valid >> (2 * i + 1)) & 1 ? p1 : 0.f;
+    }
+    hi[i] = pack_bf16x2(p0, p1);
+    const float2 r = sub_f32x2(make_float2(p0, p1), make_float2(bf16_lo(hi[i]), bf16_hi(hi[i])));
+    lo[i] = pack_bf16x2(r.x, r.y);
+  }
+}
+
+// Persistent: each CTA walks tiles blockIdx.x, + gridDim.x, ...  Every role walks the
+// same list and skips the same tiles, so their running block counters agree; the
+// loader fetches the next tile's Q and K/V while the current one computes, and the
+// MMA warp starts the next tile's S during the current epilogue.
+__global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   PfSmem &sm = *reinterpret_cast<PfSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // tile rank r (latest tiles first over the grid), then sequence, then K/V head
-  const int per_rank = a.num_seqs * kKvHeads;
-  const int rank = int(blockIdx.x) / per_rank, rem = int(blockIdx.x) % per_rank;
-  const int s = rem / kKvHeads, g = rem % kKvHeads;
-  const int tile = a.tiles_per_seq - 1 - rank;
-  const int q0 = __ldg(a.query_start + s);
-  const int n = __ldg(a.query_start + s + 1) - q0;
-  const int ctx = __ldg(a.context_lens + s);
-  const int t0 = tile * kPfTok;
-  if (n <= 0 || t0 >= n) return;
-  const int tend = min(t0 + kPfTok, n);
-  if (ctx < 0 || ctx > a.max_context || n > ctx) {
-    // invalid sequence: zero this CTA's rows (its tokens, query heads 4g .. 4g+3)
-    if (tile == 0 && g == 0 && tid == 0) report(a.status, PKV_DEV_BAD_CONTEXT);
-    for (int k = tid; k < (tend - t0) * kGroup * kHeadDim; k += kPfThreads) {
-      const int tok = t0 + k / (kGroup * kHeadDim), r = k % (kGroup * kHeadDim);
-      a.out[((long long)(q0 + tok) * kQHeads + g * kGroup) * kHeadDim + r] = 0.f;
-    }
-    return;
-  }
-  const int base_pos = ctx - n;                         // position of query token 0
-  const int last_pos = base_pos + tend - 1;             // latest position in this tile
-  const int nblocks = last_pos / kPfKeys + 1;
-  const int npages = last_pos / kPageTokens + 1;        // pages holding keys 0 .. last_pos
-  const int32_t *table = a.block_tables + (long long)s * a.bt_stride;
 
   if (tid == 0) {
-    mbar_init(&sm.q_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.q_full[i], 32);
+      mbar_init(&sm.q_empty[i], 1);
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_free[i], 1);
+    }
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(&sm.kv_full[i], 1);
       mbar_init(&sm.kv_empty[i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.s_free[b], 128);
-    }
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.p_free, 1);
+    mbar_init(&sm.p_full[0], kPfRows);
+    mbar_init(&sm.p_full[1], kPfRows);
+    mbar_init(&sm.p_free[0], 1);
+    mbar_init(&sm.p_free[1], 1);
     mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
     mbar_init_fence();
+  }
+  if (tid < kPfRows) {
+    // ones block: key row r (of 64) holds bf16 1.0 in element 0 (its 128-byte-swizzled position)
+    for (int i = tid; i < kPfKeys * 8; i += kPfRows) {
+      const int r = i >> 3, c = i & 7;
+      *reinterpret_cast<uint4 *>(sm.ones + r * kRowBytes + ((c ^ (r & 7)) << 4)) =
+          make_uint4(c == 0 ? 0x3f80u : 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
   }
   if (warp == 5) tmem_alloc(&sm.tmem_base, kPfTmemCols);
   tc_fence_before();
@@ -174,99 +225,186 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 4) {
-    // ================= TMA producer: head g's K and V rows, 4 pages per block =================
+    // ================= loader: Q rows (plain loads) and K/V blocks (tiled TMA) =================
+    const uint64_t policy = policy_evict_last();
     if (lane == 0) {
-      const uint64_t policy = policy_evict_last();
       prefetch_tensormap(&a.tmap_k);
       prefetch_tensormap(&a.tmap_v);
-      int issued = 0;
-      for (int j = 0; j < nblocks; ++j) {
-        const int st = j % kPfStages;
-        if (j >= kPfStages && !pf_wait(sm, &sm.kv_empty[st], uint32_t(j / kPfStages - 1) & 1, a.status)) break;
-        mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kPfTileBytes);
+    }
+    long long gb = 0;  // K/V blocks issued so far
+    int lt = 0;        // tiles run so far
+    bool ok = true;
+    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
+      const PfTile t = pf_tile(a, ti);
+      if (!t.run) continue;
+      const int32_t *table = a.block_tables + (long long)t.s * a.bt_stride;
+      // block-table entries of the first 128 pages: page lp sits in lane lp % 32, slot lp / 32
+      int ent[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int lp = lane + 32 * k;
+        ent[k] = lp < t.npages ? __ldg(table + lp) : -1;
+      }
+      // Q of this tile into buffer lt % 2: lane = 16-byte chunk of a token's 4 head rows
+      // (a padding token past n repeats the last real token; its rows are not written)
+      const int qb = lt & 1;
+      if (lt >= 2) {
+        const bool w = pf_wait(sm, &sm.q_empty[qb], uint32_t(lt / 2 - 1) & 1, a.status);
+        if (!__all_sync(0xffffffffu, w)) break;
+      }
+      {
+        const int hh = lane >> 3, c = lane & 7;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tok = half * 16 + i;
+            x[i] = __ldg(a.q + ((long long)(t.q0 + min(t.t0 + tok, t.n - 1)) * kQHeads + t.g * kGroup) * 8 + lane);
+            x[i].x ^= a.q_sign;
+            x[i].y ^= a.q_sign;
+            x[i].z ^= a.q_sign;
+            x[i].w ^= a.q_sign;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = 4 * (half * 16 + i) + hh;
+            *reinterpret_cast<uint4 *>(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4)) = x[i];
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.q_full[qb]);
+      }
+      for (int j = 0; j < t.nblocks; ++j, ++gb) {
+        const int st = int(gb % kPfStages);
+        if (gb >= kPfStages) {
+          const bool w = pf_wait(sm, &sm.kv_empty[st], uint32_t(gb / kPfStages - 1) & 1, a.status);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+        }
+        int page[kPfPagesPerBlock], bad = 0;
+#pragma unroll
         for (int pp = 0; pp < kPfPagesPerBlock; ++pp) {
           const int lp = j * kPfPagesPerBlock + pp;
-          int page = -1;  // outside the pool: TMA fills the box with zeros
-          if (lp < npages) {
-            page = __ldg(table + lp);
-            if (page < 0 || page >= a.num_pages) {
-              report(a.status, PKV_DEV_BAD_PAGE);
-              page = -1;
-            }
+          int e;
+          if (lp < 128) {
+            const int k = lp >> 5;
+            e = __shfl_sync(0xffffffffu, k == 0 ? ent[0] : k == 1 ? ent[1] : k == 2 ? ent[2] : ent[3], lp & 31);
+          } else {
+            e = lp < t.npages ? __ldg(table + lp) : -1;
           }
-          tma_load_3d(sm.k[st] + pp * kPfBox, &a.tmap_k, 0, g * kPageTokens, page, &sm.kv_full[st], policy);
-          tma_load_3d(sm.v[st] + pp * kPfBox, &a.tmap_v, 0, g * kPageTokens, page, &sm.kv_full[st], policy);
+          page[pp] = -1;  // outside the pool: TMA fills the box with zeros
+          if (lp < t.npages) {
+            if (e >= 0 && e < a.num_pages)
+              page[pp] = e;
+            else
+              bad |= 1 << pp;
+          }
         }
-        issued = j + 1;
+        if (lane == 0) {
+          if (bad) report(a.status, PKV_DEV_BAD_PAGE);
+          sm.kv_bad[st] = bad;
+          mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kPfTileBytes);
+#pragma unroll
+          for (int pp = 0; pp < kPfPagesPerBlock; ++pp) {
+            tma_load_3d(sm.k[st] + pp * kPfBox, &a.tmap_k, 0, t.g * kPageTokens, page[pp], &sm.kv_full[st], policy);
+            tma_load_3d(sm.v[st] + pp * kPfBox, &a.tmap_v, 0, t.g * kPageTokens, page[pp], &sm.kv_full[st], policy);
+          }
+        }
+        __syncwarp();
       }
-      // every copy issued has landed before the CTA exits
-      for (int j = max(0, issued - kPfStages); j < issued; ++j)
-        mbar_wait(&sm.kv_full[j % kPfStages], uint32_t(j / kPfStages) & 1);
+      ++lt;
     }
+    // every copy issued has landed before the CTA exits
+    if (lane == 0)
+      for (long long j = gb > kPfStages ? gb - kPfStages : 0; j < gb; ++j)
+        mbar_wait(&sm.kv_full[int(j % kPfStages)], uint32_t(j / kPfStages) & 1);
     __syncwarp();
   } else if (warp == 5) {
-    // ================= MMA issuer =================
-    const uint32_t q_base = smem_addr(sm.q), phi = smem_addr(sm.p_hi), plo = smem_addr(sm.p_lo);
-    bool ok = pf_wait(sm, &sm.q_full, 0, a.status);
-    ok = __all_sync(0xffffffffu, ok);
-    auto issue_pv = [&](int i) {
-      bool w = pf_wait(sm, &sm.p_full, uint32_t(i) & 1, a.status);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) return false;
+    // ================= MMA issuer (one thread issues, the warp waits) =================
+    long long gb = 0;          // blocks whose S was issued
+    long long pend = -1;       // block whose P V is still to issue
+    bool pend_first = false;   // ... and whether it starts its tile (O is overwritten, not accumulated)
+    int lt = 0;
+    bool ok = true;
+    auto issue_pv = [&]() {
+      bool w = pf_wait(sm, &sm.p_full[pend & 1], uint32_t(pend >> 1) & 1, a.status);
+      if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const int st = i % kPfStages;
+        const int st = int(pend % kPfStages), b = int(pend & 1);
         const uint32_t vb = smem_addr(sm.v[st]);
+        const uint32_t pa = tmem + kColS + b * kPfKeys;  // P hi in its 32 first columns, P lo in the next 32
+        const uint32_t to_ones = smem_addr(sm.ones) - vb;  // stride to the second (ones) MN atom
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tmem + kColO, sw128_desc(phi + kk * 32, 16, 1024), sw128_desc(vb + kk * 2048, 1024, 1024), kIdescPV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tmem + kColO, pa + kk * 8, sw128_desc(vb + kk * 2048, to_ones, 1024), kIdescPV,
+                        (pend_first && kk == 0) ? 0u : 1u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tmem + kColO, sw128_desc(plo + kk * 32, 16, 1024), sw128_desc(vb + kk * 2048, 1024, 1024), kIdescPV,
-                 1u);
-        tc_commit(&sm.p_free);
+          tc_mma_tmem_a(tmem + kColO, pa + 32 + kk * 8, sw128_desc(vb + kk * 2048, to_ones, 1024), kIdescPV, 1u);
+        tc_commit(&sm.p_free[b]);
         tc_commit(&sm.kv_empty[st]);
+        tc_commit(&sm.s_free[b]);
       }
       __syncwarp();
+      pend = -1;
       return true;
     };
-    for (int j = 0; ok && j < nblocks; ++j) {
-      const int st = j % kPfStages, b = j & 1;
-      bool w = pf_wait(sm, &sm.kv_full[st], uint32_t(j / kPfStages) & 1, a.status);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) break;
-      // V rows at or past the context (stale pool bytes) in this block become zeros
-      const int z0 = max(ctx, j * kPfKeys), z1 = min(npages * kPageTokens, (j + 1) * kPfKeys);
-      if (z0 < z1) {
-        uint8_t *vt = sm.v[st];
-        for (int idx = lane; idx < (z1 - z0) * 8; idx += 32)
-          *reinterpret_cast<uint4 *>(vt + (z0 - j * kPfKeys + idx / 8) * kRowBytes + (idx % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (j >= 2) {
-        w = pf_wait(sm, &sm.s_free[b], uint32_t(j / 2 - 1) & 1, a.status);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t kb = smem_addr(sm.k[st]);
+    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
+      const PfTile t = pf_tile(a, ti);
+      if (!t.run) continue;
+      const int qb = lt & 1;
+      bool w = pf_wait(sm, &sm.q_full[qb], uint32_t(lt / 2) & 1, a.status);
+      if (!__all_sync(0xffffffffu, w)) break;
+      const uint32_t q_base = smem_addr(sm.q[qb]);
+      for (int j = 0; j < t.nblocks; ++j, ++gb) {
+        const int st = int(gb % kPfStages), b = int(gb & 1);
+        w = pf_wait(sm, &sm.kv_full[st], uint32_t(gb / kPfStages) & 1, a.status);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        // V rows at or past the context (stale pool bytes) in this block become zeros
+        const int z0 = max(t.ctx, j * kPfKeys), z1 = min(t.npages * kPageTokens, (j + 1) * kPfKeys);
+        if (z0 < z1) {
+          uint8_t *vt = sm.v[st];
+          for (int idx = lane; idx < (z1 - z0) * 8; idx += 32)
+            *reinterpret_cast<uint4 *>(vt + (z0 - j * kPfKeys + idx / 8) * kRowBytes + (idx % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (gb >= 2) {
+          w = pf_wait(sm, &sm.s_free[b], uint32_t(gb / 2 - 1) & 1, a.status);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kb = smem_addr(sm.k[st]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tmem + kColS + b * kPfKeys, sw128_desc(q_base + kk * 32, 16, 1024), sw128_desc(kb + kk * 32, 16, 1024),
-                 kIdescS, kk > 0 ? 1u : 0u);
-        tc_commit(&sm.s_full[b]);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(tmem + kColS + b * kPfKeys, sw128_desc(q_base + kk * 32, 16, 1024),
+                   sw128_desc(kb + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          tc_commit(&sm.s_full[b]);
+          if (j == t.nblocks - 1) tc_commit(&sm.q_empty[qb]);  // the tile's last read of its Q
+        }
+        __syncwarp();
+        if (pend >= 0 && !issue_pv()) {
+          ok = false;
+          break;
+        }
+        pend = gb;
+        pend_first = (j == 0);
       }
-      __syncwarp();
-      if (j >= 1 && !issue_pv(j - 1)) {
-        ok = false;
-        break;
-      }
-      if (j == nblocks - 1 && !issue_pv(j)) ok = false;
+      ++lt;
     }
+    if (ok && pend >= 0) issue_pv();
     // every MMA issued has completed before the tensor memory is freed
     if (lane == 0) {
       tc_commit(&sm.mma_done);
@@ -276,102 +414,93 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
   } else {
     // ================= softmax warps: thread = row = 4 * token + head =================
     const int r = tid, tok = r >> 2, hh = r & 3;
-    {
-      // Q row (a padding row past n repeats the last real token; it is not written)
-      const uint4 *src = a.q + ((long long)(q0 + min(t0 + tok, n - 1)) * kQHeads + g * kGroup + hh) * 8;
-      uint4 c[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = __ldg(src + i);
-      put_row_sw128(sm.q, r, c);
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.q_full);
-    }
-    const int pos = base_pos + min(t0 + tok, n - 1);
     const uint32_t lane_base = tmem + (uint32_t(32 * warp) << 16);
-    float m_ref = -INFINITY, l_sum = 0.f;
+    long long gb = 0;
     bool ok = true;
-    for (int j = 0; j < nblocks; ++j) {
-      const int b = j & 1;
-      bool w = pf_wait(sm, &sm.s_full[b], uint32_t(j >> 1) & 1, a.status);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
+    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
+      const PfTile t = pf_tile(a, ti);
+      if (t.invalid) {
+        // invalid sequence: zero this tile's rows (its tokens, query heads 4g .. 4g+3)
+        if (t.t0 == 0 && t.g == 0 && tid == 0) report(a.status, PKV_DEV_BAD_CONTEXT);
+        const int rows = min(kPfTok, t.n - t.t0) * kGroup * kHeadDim;
+        for (int k = tid; k < rows; k += kPfRows)
+          a.out[((long long)(t.q0 + t.t0 + k / (kGroup * kHeadDim)) * kQHeads + t.g * kGroup) * kHeadDim +
+                k % (kGroup * kHeadDim)] = 0.f;
+        continue;
       }
-      tc_fence_after();
-      uint32_t sv[64];
-      {
-        uint32_t x0[32], x1[32];
-        tmem_ld32(lane_base + kColS + b * kPfKeys, x0);
-        tmem_ld32(lane_base + kColS + b * kPfKeys + 32, x1);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = x0[c];
-          sv[32 + c] = x1[c];
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[b]);
-      // scores in log2 units; keys after this row's position, and the keys of
-      // invalid pages (loaded as zeros), are masked
-      const int key0 = j * kPfKeys;
-      int bad = 0;
-#pragma unroll
-      for (int pp = 0; pp < kPfPagesPerBlock; ++pp) {
-        const int lp = j * kPfPagesPerBlock + pp;
-        if (lp < npages) {
-          const int page = __ldg(table + lp);
-          if (page < 0 || page >= a.num_pages) bad |= 1 << pp;
-        }
-      }
-      float x[64];
-      float mx = -INFINITY;
-      if (key0 + kPfKeys - 1 <= pos && bad == 0) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = __uint_as_float(sv[c]) * a.scale_log2;
-          mx = fmaxf(mx, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = (key0 + c <= pos && !((bad >> (c / kPageTokens)) & 1)) ? __uint_as_float(sv[c]) * a.scale_log2
-                                                                          : -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-      }
-      // move the reference max only when this block's max exceeds it by more than 2^8
-      const bool move = mx > m_ref + kRescaleLog2;
-      float alpha = 1.f;
-      if (move) {
-        alpha = exp2f(m_ref - mx);  // 0 for the first block (m_ref = -inf)
-        m_ref = mx;
-        l_sum *= alpha;
-      }
-      float psum = 0.f;
-      uint4 hi[8], lo[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t h4[4], l4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(x[8 * c + 2 * e] - m_ref), p1 = exp2f(x[8 * c + 2 * e + 1] - m_ref);
-          psum += p0 + p1;
-          h4[e] = pack_bf16x2(p0, p1);
-          l4[e] = pack_bf16x2(p0 - bf16_lo(h4[e]), p1 - bf16_hi(h4[e]));
-        }
-        hi[c] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-        lo[c] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
-      }
-      l_sum += psum;
-      if (j >= 1) {
-        // P V of the previous block has finished: P may be overwritten and O rescaled
-        w = pf_wait(sm, &sm.p_free, uint32_t(j - 1) & 1, a.status);
+      if (!t.run) continue;
+      const int pos = t.ctx - t.n + min(t.t0 + tok, t.n - 1);
+      float m_ref = -INFINITY;  // reference max of the row's unscaled scores
+      const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+      for (int j = 0; j < t.nblocks; ++j, ++gb) {
+        const int b = int(gb & 1), st = int(gb % kPfStages);
+        // S of block j, and (already complete) the stage's load, for its bad-page mask
+        bool w = pf_wait(sm, &sm.s_full[b], uint32_t(gb >> 1) & 1, a.status) &&
+                 pf_wait(sm, &sm.kv_full[st], uint32_t(gb / kPfStages) & 1, a.status);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, move)) {
+        float sv[64];
+        {
+          uint32_t x0[32], x1[32];
+          tmem_ld32(lane_base + kColS + b * kPfKeys, x0);
+          tmem_ld32(lane_base + kColS + b * kPfKeys + 32, x1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = __uint_as_float(x0[c]);
+            sv[32 + c] = __uint_as_float(x1[c]);
+          }
+        }
+        // keys after this row's position, and the keys of invalid pages (loaded as
+        // zeros), are masked: left out of the max, weight 0
+        const int key0 = j * kPfKeys;
+        const int bad = sm.kv_bad[st];
+        const bool masked = !(key0 + kPfKeys - 1 <= pos && bad == 0);
+        uint64_t valid = ~0ull;
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (!(key0 + c <= pos && !((bad >> (c / kPageTokens)) & 1))) valid &= ~(1ull << c);
+        }
+        float mx;
+        if (!masked) {
+          mx = max64(sv);
+        } else {
+          float xm[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) xm[c] = (valid >> c) & 1 ? sv[c] : -INFINITY;
+          mx = max64(xm);
+        }
+        // move the reference max only on a row's first block or when this block's max
+        // passes it by more than 8 in the exponent (a factor 2^8)
+        const bool move = j == 0 || mx > m_ref + a.move_thresh;
+        float alpha = 1.f;
+        if (move) {
+          alpha = ex2_approx((m_ref - mx) * a.scale_log2);
+          m_ref = mx;
+        }
+        // P = 2^((s - m) * scale log2 e) as bf16 hi + lo, keys 2c and 2c + 1 packed in
+        // column c (the A operand of P V); the row sum comes from P V's ones column
+        uint32_t hi[32], lo[32];
+        if (!masked)
+          block_probs<false>(sv, valid, m_ref, c2, hi, lo);
+        else
+          block_probs<true>(sv, valid, m_ref, c2, hi, lo);
+        // P overwrites this block's S in tensor memory (its S is in registers; the P V
+        // that last read this buffer finished before S was written)
+        tmem_st32(lane_base + kColS + b * kPfKeys, hi);
+        tmem_st32(lane_base + kColS + b * kPfKeys + 32, lo);
+        if (j >= 1 && __any_sync(0xffffffffu, move)) {
+          // a row's reference max moved: once the previous block's P V is done, rescale
+          // its O and row sum (before a tile's first block there is nothing to rescale)
+          w = pf_wait(sm, &sm.p_free[(gb - 1) & 1], uint32_t((gb - 1) >> 1) & 1, a.status);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t o[32];
@@ -380,25 +509,25 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
             tmem_st32(lane_base + kColO + 32 * half, o);
           }
+          tmem_st1(lane_base + kColO + kHeadDim,
+                   __float_as_uint(__uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim)) * alpha));
         }
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[b]);
       }
-      put_row_sw128(sm.p_hi, r, hi);
-      put_row_sw128(sm.p_lo, r, lo);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full);
-    }
-    // ---- epilogue: O / l for the rows of real query tokens ----
-    bool w = ok && pf_wait(sm, &sm.p_free, uint32_t(nblocks - 1) & 1, a.status);
-    if (__all_sync(0xffffffffu, w)) {
+      if (!ok) break;
+      // ---- epilogue: O / l for the rows of real query tokens ----
+      const bool w = pf_wait(sm, &sm.p_free[(gb - 1) & 1], uint32_t((gb - 1) >> 1) & 1, a.status);
+      if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
+      const float l_sum = __uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim));
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      float *dst = a.out + ((long long)(q0 + t0 + tok) * kQHeads + g * kGroup + hh) * kHeadDim;
+      float *dst = a.out + ((long long)(t.q0 + t.t0 + tok) * kQHeads + t.g * kGroup + hh) * kHeadDim;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t o[32];
         tmem_ld32(lane_base + kColO + 32 * half, o);
-        if (t0 + tok < n) {
+        if (t.t0 + tok < t.n) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
             *reinterpret_cast<float4 *>(dst + 32 * half + c) =
@@ -406,6 +535,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) paged_prefill_kernel(const __gr
                             __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
         }
       }
+      tc_fence_before();  // the reads of O precede the next tile's first P V (ordered by p_full)
     }
   }
   tc_fence_before();
@@ -461,9 +591,14 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   a.num_seqs = num_seqs;
   a.max_context = max_context;
   a.tiles_per_seq = int(tiles);
-  a.scale_log2 = scale * pkv::kLog2e;
+  a.scale_log2 = fabsf(scale) * pkv::kLog2e;
+  a.move_thresh = a.scale_log2 > 0.f ? pkv::kRescaleLog2 / a.scale_log2 : INFINITY;
+  a.q_sign = scale < 0.f ? 0x80008000u : 0u;
   a.status = device_status;
-  const unsigned grid = unsigned((long long)num_seqs * tiles * pkv::kKvHeads);
+  a.num_tiles = int((long long)num_seqs * tiles * pkv::kKvHeads);
+  const int sms = pkv::device_sm_count();
+  const int resident = (sms > 0 ? sms : 148) * pkv::kPfCtasPerSm;
+  const unsigned grid = unsigned(a.num_tiles < resident ? a.num_tiles : resident);
   pkv::paged_prefill_kernel<<<grid, pkv::kPfThreads, pkv::kPfSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }

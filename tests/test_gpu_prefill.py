@@ -24,8 +24,9 @@ def _gpu():
         pytest.skip("no CUDA device")
 
 
-def _run(wl, nq, seed=1, bt=None):
+def _run(wl, nq, seed=1, bt=None, scale=None):
     """Queries = the last nq[s] tokens of each sequence (all already appended)."""
+    scale = wl.scale if scale is None else scale
     import paged_kv_cache_180_gb300 as pkv
     d = U.DeviceDecode(wl)
     d.append_all()
@@ -35,12 +36,12 @@ def _run(wl, nq, seed=1, bt=None):
     out = torch.full((max(total, 1), 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
     bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :] if bt is None else bt)
     pkv.paged_prefill_attention(d.pool, out, U.to_dev(qbits), U.to_dev(qs), U.to_dev(bt_host), bt_host.shape[1],
-                                d.lens, max(max(nq), 1), wl.max_context, wl.scale, d.status)
+                                d.lens, max(max(nq), 1), wl.max_context, scale, d.status)
     got = out[:total].cpu().double().numpy()
     opool = oracle.Pool(wl.num_pages)
     k, v, slots = wl.kv_all(0)
     oracle.kv_append(opool, k, v, slots)
-    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, scale, wl.max_context)
     return got, ref, err, d.status_value(), qs
 
 
@@ -93,3 +94,14 @@ def test_page_permutation_bit_exact():
     wl2 = configs.DecodeWorkload(wl.name, wl.seed, wl.num_pages, 1, wl.context_lens, bt2)
     got2, _, _, _, _ = _run(wl2, [60, 90])
     assert np.array_equal(got1.astype(np.float32).view(np.int32), got2.astype(np.float32).view(np.int32))
+
+
+@pytest.mark.parametrize("scale", [1.0, -1.0, -0.125, 0.0])
+def test_scales_moving_max_and_sign(scale):
+    # scale 1: scores spread ~8x wider than at 1/sqrt(64), so a row's running maximum
+    # jumps by more than 2^8 after its first key block and the kernel must rescale O and
+    # the row sum; negative scales flip which keys dominate; scale 0 is a uniform average
+    wl = configs.custom(607, [700, 300, 64], name="scales")
+    got, ref, err, st, _ = _run(wl, [700, 150, 64], scale=scale)
+    assert err == 0 and st == 0
+    U.assert_close(got, ref, f"scale {scale}")
