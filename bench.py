@@ -698,31 +698,65 @@ def run_prefill(args):
     def attend():
         pkv.paged_prefill_attention(pool, out, q, qs, bt, bt.shape[1], lens, plen, wl.max_context, wl.scale, status)
 
-    for _ in range(warmup):
-        pkv.kv_append(pool, k, v, slots, status)
+    def step(attention_only=False):
+        if not attention_only:
+            pkv.kv_append(pool, k, v, slots, status)
         attend()
+
+    for _ in range(warmup):
+        step()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # Each step replays as a CUDA graph (whole step, and attention alone for the per-kernel
+    # figure), so host-side call overhead never shows up as device idle time.
+    use_graph = args.graph != "off"
+    graphs = None
+    if use_graph:
+        graphs = []
+        for attention_only in (False, True):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(attention_only=attention_only)
+            graphs.append(g)
+        for _ in range(3):
+            graphs[0].replay()
+            graphs[1].replay()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(dev)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     tw0 = time.time()
-    for e in ev:
-        flush_w.zero_()
-        flush_r.max()
-        e[0].record(stream)
-        pkv.kv_append(pool, k, v, slots, status)
-        e[1].record(stream)
-        attend()
-        e[2].record(stream)
-    torch.cuda.synchronize()
+    if graphs is None:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for e in ev:
+            flush_w.zero_()
+            flush_r.max()
+            e[0].record(stream)
+            pkv.kv_append(pool, k, v, slots, status)
+            e[1].record(stream)
+            attend()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        att_ms = [e[1].elapsed_time(e[2]) for e in ev]
+        all_ms = [a + b for a, b in zip(app_ms, att_ms)]
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * steps)]
+        for i in range(2 * steps):
+            flush_w.zero_()
+            flush_r.max()
+            ev[i][0].record(stream)
+            graphs[0 if i < steps else 1].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        all_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+        att_ms = [ev[steps + i][0].elapsed_time(ev[steps + i][1]) for i in range(steps)]
+        app_ms = [max(0.0, a - b) for a, b in zip(all_ms, att_ms)]
     tw1 = time.time()
     time.sleep(0.25)
     sampler.stop()
-    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    att_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_ms = max_over_ranks(sum(a + b for a, b in zip(app_ms, att_ms)) / steps, dev)
+    step_ms = max_over_ranks(sum(all_ms) / steps, dev)
     flops = 4 * 64 * 32 * nseq * (plen * (plen + 1) // 2)
     att_s = sum(att_ms) / steps * 1e-3
     tflops = flops / att_s / 1e12
@@ -740,16 +774,19 @@ def run_prefill(args):
                 "data": "synthetic (seeded N(0,1) bf16)",
                 "config": {"workload": "prefill", "num_seqs": nseq, "prompt_tokens": plen, "layers": 1,
                            "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
-                           "l2": "L2 flushed between steps (write of a 2x L2 buffer, then read of another)"},
+                           "l2": "L2 flushed between steps (write of a 2x L2 buffer, then read of another)",
+                           "timing": ("CUDA graph replay per step (whole step; attention-only graph for the "
+                                      "per-kernel figure)" if graphs is not None else "CUDA events around each kernel")},
                 "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                              "frac": round(tflops / peak, 4), "traffic": None,
                              "kernel": "paged_prefill_kernel (tcgen05.mma M128 N64, TMEM accumulators, P as bf16 hi + lo)",
                              "algorithmic_flops_per_launch": flops,
                              "avg_launch_us": round(att_s * 1e6, 3),
                              "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json, cuBLAS burst)"},
-                "kernel_us": {"kv_append (all prompt tokens)": round(1e3 * sum(app_ms) / steps, 3),
+                "kernel_us": {("kv_append (all prompt tokens)" if graphs is None else "kv_append (step minus attention)"):
+                              round(1e3 * sum(app_ms) / steps, 3),
                               "paged_prefill_attention": round(att_s * 1e6, 3)},
-                "clocks": sampler.summary(tw0, tw1), "gpu_launches": 2 * steps}
+                "clocks": sampler.summary(tw0, tw1), "gpu_launches": 2 * steps + (steps if graphs is not None else 0)}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -97,6 +97,17 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
       : "memory");
 }
 
+// ---- cp.async: 16-byte global -> shared copies, completion signalled on an mbarrier ----
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// One arrival on the mbarrier (counted in its expected arrivals) once all of this
+// thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // ---- tiled (tensor) TMA load of a 3-D box, completion counted on an mbarrier ----
 // The x coordinate is always 0 here (whole 128-byte rows), so it is 16-byte aligned.
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
@@ -310,6 +321,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // ---- bf16 unpacking (exact widening) --------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 32-byte store of eight floats (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float *dst, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
 
 __device__ __forceinline__ void report(int32_t *status, uint32_t bits) {
   if (status != nullptr) atomicOr(reinterpret_cast<unsigned int *>(status), bits);

@@ -63,12 +63,13 @@ constexpr int kPfBox = kPageTokens * kRowBytes;        // one head's rows of one
 constexpr int kPfTileBytes = kPfKeys * kRowBytes;      // K (or V) of one block: 8 KiB
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kColS = 0;                          // S buffers at columns 0 and 64
-constexpr uint32_t kColO = 128;                        // O: columns 128 .. 191, row sum l at 192, 193 .. 255 zero
+constexpr uint32_t kColO = 128;                        // O: columns 128 .. 191, row sum l at 192 (193 .. 207 zero)
+constexpr int kPvN = kHeadDim + 16;                    // P V's N: V's 64 columns and 16 of the ones atom
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;                    // move a row's reference max when exceeded by more
 
 constexpr uint32_t kIdescS = idesc_bf16(kPfRows, kPfKeys, false);   // B = K rows (K-major)
-constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, 2 * kHeadDim, true);  // B = [V | ones] (MN-major)
+constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, kPvN, true);  // B = [V | ones] (MN-major)
 
 struct PrefillArgs {
   CUtensorMap tmap_k;  // boxes of one head's 16 rows of one page
@@ -86,7 +87,7 @@ struct PrefillArgs {
   int num_tiles;  // num_seqs * tiles_per_seq * 8
   float scale_log2;   // |scale| * log2(e)
   float move_thresh;  // scores (unscaled) by which a block's max must pass the reference to move it
-  uint32_t q_sign;    // 0x80008000 when scale < 0: Q is negated on load, so the scores use |scale|
+  int neg;            // scale < 0: a row's reference is the max of -s (the min of s)
   int32_t *status;
 };
 
@@ -149,16 +150,27 @@ __device__ __forceinline__ bool pf_wait(PfSmem &sm, uint64_t *bar, uint32_t pari
   return false;
 }
 
-// Largest of 64 values (a tree, so the chain is 6 deep).
-__device__ __forceinline__ float max64(const float (&x)[64]) {
+// Largest (kMin: smallest) of 64 values, as a tree so the chain is 6 deep.
+template <bool kMin>
+__device__ __forceinline__ float extreme64(const float (&x)[64]) {
   float m[32];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) m[c] = fmaxf(x[c], x[c + 32]);
+  for (int c = 0; c < 32; ++c) m[c] = kMin ? fminf(x[c], x[c + 32]) : fmaxf(x[c], x[c + 32]);
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
-    for (int c = 0; c < w; ++c) m[c] = fmaxf(m[c], m[c + w]);
+    for (int c = 0; c < w; ++c) m[c] = kMin ? fminf(m[c], m[c + w]) : fmaxf(m[c], m[c + w]);
   return m[0];
+}
+
+// max over the keys whose bit in `valid` is set of sigma * s, sigma = -1 when neg.
+__device__ __forceinline__ float signed_max(const float (&sv)[64], bool masked, uint64_t valid, bool neg) {
+  if (!masked) return neg ? -extreme64<true>(sv) : extreme64<false>(sv);
+  float xm[64];
+  const float off = neg ? INFINITY : -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) xm[c] = (valid >> c) & 1 ? sv[c] : off;
+  return neg ? -extreme64<true>(xm) : extreme64<false>(xm);
 }
 
 // P = 2^((s - m) * c) for the 64 keys of a block as bf16 hi + lo parts, keys 2i and
@@ -253,27 +265,16 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         if (!__all_sync(0xffffffffu, w)) break;
       }
       {
+        // asynchronous 16-byte copies; q_full counts one arrival per lane once its copies land
         const int hh = lane >> 3, c = lane & 7;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 x[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int tok = half * 16 + i;
-            x[i] = __ldg(a.q + ((long long)(t.q0 + min(t.t0 + tok, t.n - 1)) * kQHeads + t.g * kGroup) * 8 + lane);
-            x[i].x ^= a.q_sign;
-            x[i].y ^= a.q_sign;
-            x[i].z ^= a.q_sign;
-            x[i].w ^= a.q_sign;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = 4 * (half * 16 + i) + hh;
-            *reinterpret_cast<uint4 *>(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4)) = x[i];
-          }
+        const uint4 *src = a.q + ((long long)t.q0 * kQHeads + t.g * kGroup) * 8 + lane;
+#pragma unroll 8
+        for (int tok = 0; tok < kPfTok; ++tok) {
+          const int r = 4 * tok + hh;
+          cp_async_16(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4),
+                      src + (long long)min(t.t0 + tok, t.n - 1) * kQHeads * 8);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.q_full[qb]);
+        cp_async_arrive(&sm.q_full[qb]);
       }
       for (int j = 0; j < t.nblocks; ++j, ++gb) {
         const int st = int(gb % kPfStages);
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       const int qb = lt & 1;
       bool w = pf_wait(sm, &sm.q_full[qb], uint32_t(lt / 2) & 1, a.status);
       if (!__all_sync(0xffffffffu, w)) break;
+      fence_proxy_async_smem();  // Q landed through the generic proxy; the MMAs read it through the async one
       const uint32_t q_base = smem_addr(sm.q[qb]);
       for (int j = 0; j < t.nblocks; ++j, ++gb) {
         const int st = int(gb % kPfStages), b = int(gb & 1);
@@ -430,8 +432,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       }
       if (!t.run) continue;
       const int pos = t.ctx - t.n + min(t.t0 + tok, t.n - 1);
-      float m_ref = -INFINITY;  // reference max of the row's unscaled scores
-      const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+      // reference max of the row's sigma * s (sigma = sign of scale): the exponents are
+      // |scale| log2(e) (sigma s - m) = (sigma |scale| log2(e)) (s - sigma m)
+      float m_ref = -INFINITY;
+      const float sig = a.neg ? -1.f : 1.f;
+      const float2 c2 = make_float2(sig * a.scale_log2, sig * a.scale_log2);
       for (int j = 0; j < t.nblocks; ++j, ++gb) {
         const int b = int(gb & 1), st = int(gb % kPfStages);
         // S of block j, and (already complete) the stage's load, for its bad-page mask
@@ -464,15 +469,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
           for (int c = 0; c < 64; ++c)
             if (!(key0 + c <= pos && !((bad >> (c / kPageTokens)) & 1))) valid &= ~(1ull << c);
         }
-        float mx;
-        if (!masked) {
-          mx = max64(sv);
-        } else {
-          float xm[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c) xm[c] = (valid >> c) & 1 ? sv[c] : -INFINITY;
-          mx = max64(xm);
-        }
+        const float mx = signed_max(sv, masked, valid, a.neg != 0);  // in units of sigma * s
         // move the reference max only on a row's first block or when this block's max
         // passes it by more than 8 in the exponent (a factor 2^8)
         const bool move = j == 0 || mx > m_ref + a.move_thresh;
@@ -485,9 +482,9 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         // column c (the A operand of P V); the row sum comes from P V's ones column
         uint32_t hi[32], lo[32];
         if (!masked)
-          block_probs<false>(sv, valid, m_ref, c2, hi, lo);
+          block_probs<false>(sv, valid, sig * m_ref, c2, hi, lo);
         else
-          block_probs<true>(sv, valid, m_ref, c2, hi, lo);
+          block_probs<true>(sv, valid, sig * m_ref, c2, hi, lo);
         // P overwrites this block's S in tensor memory (its S is in registers; the P V
         // that last read this buffer finished before S was written)
         tmem_st32(lane_base + kColS + b * kPfKeys, hi);
@@ -523,16 +520,28 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       const float l_sum = __uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim));
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       float *dst = a.out + ((long long)(t.q0 + t.t0 + tok) * kQHeads + t.g * kGroup + hh) * kHeadDim;
+      const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t o[32];
         tmem_ld32(lane_base + kColO + 32 * half, o);
         if (t.t0 + tok < t.n) {
+          if (wide) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4 *>(dst + 32 * half + c) =
-                make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                            __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+            for (int c = 0; c < 32; c += 8) {
+              const float v[8] = {__uint_as_float(o[c]) * inv,     __uint_as_float(o[c + 1]) * inv,
+                                  __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv,
+                                  __uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv,
+                                  __uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv};
+              st_global_v8(dst + 32 * half + c, v);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4 *>(dst + 32 * half + c) =
+                  make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                              __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+          }
         }
       }
       tc_fence_before();  // the reads of O precede the next tile's first P V (ordered by p_full)
@@ -593,7 +602,7 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   a.tiles_per_seq = int(tiles);
   a.scale_log2 = fabsf(scale) * pkv::kLog2e;
   a.move_thresh = a.scale_log2 > 0.f ? pkv::kRescaleLog2 / a.scale_log2 : INFINITY;
-  a.q_sign = scale < 0.f ? 0x80008000u : 0u;
+  a.neg = scale < 0.f ? 1 : 0;
   a.status = device_status;
   a.num_tiles = int((long long)num_seqs * tiles * pkv::kKvHeads);
   const int sms = pkv::device_sm_count();
