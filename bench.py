@@ -253,8 +253,9 @@ def run_reference(args):
             "warmup": warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 K/V/q)",
             "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "layers": wl.num_layers,
-                       "context": "per-sequence lengths of the workload", "q_heads": 32, "kv_heads": 8,
-                       "head_dim": 64, "page_tokens": 16, "parallelism": "host threads", "l2": "n/a (CPU)"},
+                       "context_lens": ("2048 each" if wl.name == "bandwidth" else "per workload"),
+                       "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
+                       "pool_pages": wl.num_pages, "parallelism": "host threads", "l2": "n/a (CPU)"},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"each step: the whole {wl.name} step (append + FP64 attention of every "
