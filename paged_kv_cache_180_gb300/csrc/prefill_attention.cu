@@ -12,31 +12,36 @@
 //   p_i = context_lens[s] - n_s + (i - query_start[s])
 //
 // GB300 design (tcgen05 tensor cores, accumulators in tensor memory)
-//  * Tile: one CTA per (32 query tokens of a sequence, K/V head g).  Its 128 rows
-//    (row = 4 * token + head in group) share every K/V row it loads: M = 128.
-//    Tiles are numbered latest-first over the whole grid, so the longest causal
-//    spans start first.
+//  * Tile: 32 query tokens of a sequence against one K/V head g.  Its 128 rows
+//    (row = 4 * token + head in group) share every K/V row loaded: M = 128.  The
+//    grid is persistent (two CTAs per SM); each CTA walks the tiles blockIdx.x,
+//    + gridDim.x, ..., numbered latest-first so the longest causal spans start first.
 //  * Keys in blocks of 64 (4 pages).  S = Q K^T is 4 tcgen05.mma (M 128, N 64,
-//    K 16 each; Q and K K-major, 128-byte swizzled) into one of two TMEM
-//    buffers, so S of block j + 1 runs while the softmax reads block j.
-//    O += P V is 8 tcgen05.mma into a TMEM accumulator: P is split into bf16
-//    hi + lo halves (weights keep ~16 significant bits), both multiplied by the
-//    same V tile (MN-major, 128-byte swizzled).
-//  * Warp roles: warps 0-3 own one row each per thread (TMEM lane = row): they
-//    load Q, read S from TMEM, mask, keep the row's running max and sum, write P
-//    to shared memory and finally read O, divide and store.  Warp 4 streams head
-//    g's K and V rows of each page with tiled TMA (2 KiB boxes) into a 3-stage
-//    ring; pages past the query span are loaded from a coordinate outside the
-//    pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and
-//    issues the MMAs (one thread), completion signalled by tcgen05.commit.
+//    K 16; Q and K K-major, 128-byte swizzled) into one of two TMEM S buffers, so
+//    S of block j + 1 runs while the softmax works on block j.  P, as bf16 hi + lo
+//    halves (the weights keep ~16 significant bits), is stored back over its own S
+//    and read by O += P V as the TMEM A operand: 8 tcgen05.mma of N 80, B being V
+//    (MN-major, 128-byte swizzled) followed by 16 columns of a constant "ones" atom,
+//    so O's column 64 accumulates the row sum of exactly the weights used.
+//  * Warp roles: warps 0-3 own one row each per thread (TMEM lane = row): they read
+//    S, mask, keep the row's reference maximum, write P, and finally read O, divide
+//    and store.  Warp 4 loads: the next tile's Q rows by cp.async (two Q buffers)
+//    and head g's K and V rows of each page by tiled TMA (2 KiB boxes) into a
+//    4-stage ring; pages past the query span come from a coordinate outside the
+//    pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and issues
+//    the MMAs from one thread (S of block j, then P V of block j - 1), completion
+//    signalled by tcgen05.commit.
 //  * Online softmax in the exp2 domain with a lazily moved maximum: a row's
-//    reference maximum moves only when a block's maximum exceeds it by more than
-//    8 (a factor 256), and only then is the row of O in TMEM rescaled (after the
-//    previous P V completed).  The final division by the row sum uses the same
-//    reference, so the result is the exact softmax up to rounding.
-//  * Masks: key t counts for a row at position p when t <= p (p < ctx); other
-//    scores become -inf.  V rows at or past the context in a sequence's last page
-//    are zeroed in shared memory so stale pool bytes (even NaN) never reach O.
+//    reference moves only when a block's maximum exceeds it by more than 8 (a
+//    factor 256), and only then is the row of O (with its sum column) rescaled in
+//    TMEM, after the previous P V completed.  The final division uses the same
+//    reference, so the result is the exact softmax up to rounding.  A negative
+//    scale takes the reference from -s.
+//  * Masks: keys after a row's position and the keys of invalid pages get weight 0;
+//    V rows at or past the context in a sequence's last page are zeroed in shared
+//    memory so stale pool bytes (even NaN) never reach O.
+//  * The P-ready and P V-done barriers exist per P buffer: with a single barrier a
+//    softmax warp already on the next block could complete a phase for a slower warp.
 //  * Every mbarrier wait is bounded (about 2 s): on expiry the CTA reports
 //    PKV_DEV_TIMEOUT, stops issuing work, waits (bounded) for what is in flight,
 //    frees its tensor memory and exits.
