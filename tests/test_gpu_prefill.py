@@ -105,3 +105,15 @@ def test_scales_moving_max_and_sign(scale):
     got, ref, err, st, _ = _run(wl, [700, 150, 64], scale=scale)
     assert err == 0 and st == 0
     U.assert_close(got, ref, f"scale {scale}")
+
+
+def test_invalid_page_inside_a_span():
+    # a block-table entry past the pool inside sequence 0's span: the device flags it and
+    # leaves that page out (finite rows); the other sequence of the launch is unaffected
+    wl = configs.custom(608, [200, 90], name="badpage")
+    bt = np.ascontiguousarray(wl.block_tables[:, 0, :]).copy()
+    bt[0, 5] = wl.num_pages + 7
+    got, ref, err, st, qs = _run(wl, [64, 90], bt=bt)
+    assert st & 4 and err & 4
+    assert np.isfinite(got[qs[0]:qs[1]]).all()
+    U.assert_close(got[qs[1]:qs[2]], ref[qs[1]:qs[2]], "sequence beside the invalid page")
