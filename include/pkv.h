@@ -251,7 +251,7 @@ int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches)
  * synchronise the device and fail under memory pressure mid-run).  This entry point
  * takes the same inputs and output but no workspace: the split-context partial states
  * live in one fixed array of device memory inside this library, sized for
- * PKV_NOALLOC_MAX_SEQS sequences (about 12.4 MiB), which every GPU that loads the
+ * PKV_NOALLOC_MAX_SEQS sequences (about 12.5 MiB), which every GPU that loads the
  * library holds until the process exits.  It calls no allocator.
  *
  *  - num_seqs > PKV_NOALLOC_MAX_SEQS returns PKV_ERR_NOALLOC_LIMIT and enqueues nothing.

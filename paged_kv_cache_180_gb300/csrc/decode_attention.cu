@@ -73,6 +73,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kCtasPerSm = 2;
 constexpr int kMinPagesPerCta = 4;  // least pages a CTA is given (unless the caller fixes the split)
+constexpr int kMergeGroup = 8;      // a sequence cut into more parts merges them in groups of this many first
 constexpr int kHeadRowsBytes = kPageTokens * kRowBytes;  // one head's K (or V) rows of a page: 2 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -81,7 +82,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Slot {
   float acc[kQHeads][kHeadDim];  // un-normalised sum of p * V
   float2 ml[kQHeads];            // (running max in log2 units, sum of p)
-  int counter[kWarps];           // per head group: CTAs of the sequence done so far; 0 between calls
+  int counter[kWarps];           // per head group: parts of the sequence (or of a merge group) done; 0 between calls
+  int counter2[kWarps];          // per head group: merge groups of the sequence done (long sequences); 0 between calls
 };
 
 struct DecodeArgs {
@@ -238,44 +240,55 @@ __device__ __forceinline__ void issue_page(const DecodeArgs &a, Smem &sm, int st
   }
 }
 
-// Warp g's share of finishing sequence s, cut across CTAs (its pages are the
-// global pages gfirst .. gfirst + n - 1), once this CTA's partial state is stored:
-// a ticket on the (sequence, head group) counter - an acquire-release atomic that
-// publishes the lanes' partial stores (ordered before it by __syncwarp) and, for
-// the last ticket, makes the other CTAs' partials visible.  ticket_of() takes the
-// ticket; merge_if_last() lets the warp holding the last ticket merge the partial
-// states of query heads 4g .. 4g+3 with
+// Warp g's share of finishing sequence s, cut across CTAs c_first .. c_last (its pages
+// are the global pages gfirst .. gfirst + n - 1), once this CTA's partial state is
+// stored: a ticket on a (merge group, head group) counter - an acquire-release atomic
+// that publishes the lanes' partial stores (ordered before it by __syncwarp) and, for
+// the last ticket, makes the other parts visible.  ticket_of() takes the ticket;
+// merge_if_last() lets the warp holding the last ticket merge the partial states of
+// query heads 4g .. 4g+3 with
 //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  out = sum_c acc_c 2^(m_c - M) / L
-// (one pass, rescaling as the running maximum grows) and reset the counter.  The
-// two halves may be apart: a warp can take the ticket, stream more pages, and only
-// then look at it.
-__device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long gfirst, int g, int lane, long long T,
-                                         int Gu) {
+// (one pass, rescaling as the running maximum grows) and reset the counter.  A sequence
+// in at most kMergeGroup parts is merged at once.  A longer one is merged in two levels,
+// so that no warp reads more than kMergeGroup parts in a row: the parts of each group of
+// kMergeGroup consecutive CTAs are merged into the group's first slot, and the warp that
+// finishes the last group merges the group results.  The two halves of a ticket may be
+// apart: a warp can take the ticket, stream more pages, and only then look at it.
+
+// First-level merge group [lo, hi] of part c of a sequence cut across c_first .. c_last.
+__device__ __forceinline__ void merge_group(int c, int c_first, int c_last, int &lo, int &hi) {
+  if (c_last - c_first < kMergeGroup) {
+    lo = c_first;
+    hi = c_last;
+    return;
+  }
+  lo = c_first + (c - c_first) / kMergeGroup * kMergeGroup;
+  hi = min(lo + kMergeGroup - 1, c_last);
+}
+
+__device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long gfirst, int n, int g, int lane,
+                                         long long T, int Gu, int cta) {
   __syncwarp();
   int ticket = 0;
-  if (lane == 0) ticket = atomic_add_acq_rel_gpu(&a.slots[(long long)cta_of_page(gfirst, T, Gu) + s].counter[g], 1);
+  if (lane == 0) {
+    int lo, hi;
+    merge_group(cta, cta_of_page(gfirst, T, Gu), cta_of_page(gfirst + n - 1, T, Gu), lo, hi);
+    ticket = atomic_add_acq_rel_gpu(&a.slots[(long long)lo + s].counter[g], 1);
+  }
   return ticket;  // meaningful in lane 0
 }
 
-__device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long long gfirst, int n, int g, int lane,
-                                              long long T, int Gu, int ticket) {
-  const int c_first = cta_of_page(gfirst, T, Gu);
-  const int c_last = cta_of_page(gfirst + n - 1, T, Gu);
-  int last = 0;
-  if (lane == 0) {
-    last = (ticket == c_last - c_first);  // every CTA in the span owns pages of the sequence
-    if (last) atomicExch(&a.slots[(long long)c_first + s].counter[g], 0);  // ready for the next call
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __syncwarp();  // lane 0's acquire comes before every lane's reads of the partial states
-  // lane -> query head 4g + lane/8, dims 8 (lane%8) .. +7
-  const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
-  float M = -INFINITY, L = 0.f;
-  float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+// Merge of the partial states in slots first + k * stride + s, k < count, for this lane's
+// query head h and dims d0 .. d0 + 7: the running maximum M, sum L and accumulator r.
+__device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int first, int count, int stride, int h,
+                                            int d0, float &M, float &L, float (&r)[8]) {
+  M = -INFINITY;
+  L = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = 0.f;
 #pragma unroll 8
-  for (int c = c_first; c <= c_last; ++c) {
-    const Slot &part = a.slots[(long long)c + s];
+  for (int k = 0; k < count; ++k) {
+    const Slot &part = a.slots[(long long)first + (long long)k * stride + s];
     const float2 ml = __ldcg(&part.ml[h]);
     const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
     const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
@@ -290,10 +303,49 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long l
     r[6] = r[6] * keep + wgt * x1.z; r[7] = r[7] * keep + wgt * x1.w;
     M = m_new;
   }
+}
+
+__device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long long gfirst, int n, int g, int lane,
+                                              long long T, int Gu, int ticket, int cta) {
+  const int c_first = cta_of_page(gfirst, T, Gu);
+  const int c_last = cta_of_page(gfirst + n - 1, T, Gu);
+  int lo, hi;
+  merge_group(cta, c_first, c_last, lo, hi);
+  int last = 0;
+  if (lane == 0) {
+    last = (ticket == hi - lo);  // every CTA in the group owns pages of the sequence
+    if (last) atomicExch(&a.slots[(long long)lo + s].counter[g], 0);  // ready for the next call
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __syncwarp();  // lane 0's acquire comes before every lane's reads of the partial states
+  // lane -> query head 4g + lane/8, dims 8 (lane%8) .. +7
+  const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
+  float M, L, r[8];
+  merge_parts(a, s, lo, hi - lo + 1, 1, h, d0, M, L, r);
+  if (c_last - c_first >= kMergeGroup) {
+    // first level done: the group's merged state replaces its first part, then the
+    // second-level ticket (lane 0's release covers every lane's stores after __syncwarp)
+    Slot &dst = a.slots[(long long)lo + s];
+    __stcg(reinterpret_cast<float4 *>(&dst.acc[h][d0]), make_float4(r[0], r[1], r[2], r[3]));
+    __stcg(reinterpret_cast<float4 *>(&dst.acc[h][d0 + 4]), make_float4(r[4], r[5], r[6], r[7]));
+    if ((lane & 7) == 0) __stcg(&dst.ml[h], make_float2(M, L));
+    __syncwarp();
+    const int groups = (c_last - c_first) / kMergeGroup + 1;
+    int last2 = 0;
+    if (lane == 0) {
+      last2 = atomic_add_acq_rel_gpu(&a.slots[(long long)c_first + s].counter2[g], 1) == groups - 1;
+      if (last2) atomicExch(&a.slots[(long long)c_first + s].counter2[g], 0);
+    }
+    last2 = __shfl_sync(0xffffffffu, last2, 0);
+    if (!last2) return;
+    __syncwarp();
+    merge_parts(a, s, c_first, groups, kMergeGroup, h, d0, M, L, r);
+  }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  float4 *dst = reinterpret_cast<float4 *>(a.out + ((long long)s * kQHeads + h) * kHeadDim + d0);
-  dst[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
-  dst[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+  float4 *out = reinterpret_cast<float4 *>(a.out + ((long long)s * kQHeads + h) * kHeadDim + d0);
+  out[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
+  out[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
@@ -562,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
             *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
           if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
         }
-        const int ticket = ticket_of(a, w.s, gfirst, g, lane, T, Gu);
+        const int ticket = ticket_of(a, w.s, gfirst, w.n, g, lane, T, Gu, cta);
         if (has_first || i == count - 1) {
-          merge_if_last(a, w.s, gfirst, w.n, g, lane, T, Gu, ticket);
+          merge_if_last(a, w.s, gfirst, w.n, g, lane, T, Gu, ticket, cta);
         } else {
           // The range began inside this sequence: look at the ticket after the loop,
           // so its round trip (and a merge) do not stall the pages that follow.
@@ -588,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       w.next(a);
     }
   }
-  if (pend_s >= 0) merge_if_last(a, pend_s, pend_gfirst, pend_n, g, lane, T, Gu, pend_ticket);
+  if (pend_s >= 0) merge_if_last(a, pend_s, pend_gfirst, pend_n, g, lane, T, Gu, pend_ticket, cta);
   named_barrier_sync(1, kThreads);
   if (tid == 0 && sm.any_aborted) {
     // Copies issued for pages nobody consumed: wait (bounded) so none lands after exit.

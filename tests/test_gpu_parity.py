@@ -233,9 +233,9 @@ def test_one_workspace_across_batch_sizes_and_splits():
         ref, err, _ = oracle.decode_workload(wl)
         U.assert_close(out, ref, f"batch {n}, ctas {ctas}")
         assert d.status_value() == 0
-    # every completed call leaves the counters at zero
-    slot_bytes = 32 * 64 * 4 + 32 * 8 + 8 * 4
-    counters = ws.view(-1, slot_bytes)[:, slot_bytes - 32:].contiguous().view(torch.int32)
+    # every completed call leaves both levels of merge counters at zero
+    slot_bytes = 32 * 64 * 4 + 32 * 8 + 2 * 8 * 4
+    counters = ws.view(-1, slot_bytes)[:, slot_bytes - 64:].contiguous().view(torch.int32)
     assert int(counters.abs().sum().item()) == 0
 
 
