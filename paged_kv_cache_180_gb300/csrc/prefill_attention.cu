@@ -64,6 +64,7 @@ constexpr int kPfPagesPerBlock = kPfKeys / kPageTokens;
 constexpr int kPfStages = 4;                           // K/V blocks in flight
 constexpr int kPfThreads = 192;                        // warps 0-3 softmax, 4 loads, 5 MMA
 constexpr int kPfCtasPerSm = 2;
+constexpr int kPfMaxTiles = 64;                        // tiles one CTA walks (its tile table in shared memory)
 constexpr int kPfBox = kPageTokens * kRowBytes;        // one head's rows of one page: 2 KiB
 constexpr int kPfTileBytes = kPfKeys * kRowBytes;      // K (or V) of one block: 8 KiB
 constexpr uint32_t kPfTmemCols = 256;
@@ -96,6 +97,13 @@ struct PrefillArgs {
   int32_t *status;
 };
 
+// One work tile: 32 query tokens of sequence s (from t0) against K/V head g.
+struct PfTile {
+  int s, g, t0, n, q0, ctx, nblocks, npages;
+  int run;      // has queries and a valid context
+  int invalid;  // has queries, invalid context: its rows are zeroed
+};
+
 struct __align__(1024) PfSmem {
   uint8_t q[2][kPfRows * kRowBytes];       // two tiles' Q, row = 4 * token + head, 128-byte swizzled
   uint8_t k[kPfStages][kPfTileBytes];      // 64 keys x 128 B per stage
@@ -113,17 +121,11 @@ struct __align__(1024) PfSmem {
                        // per buffer so that the phase waited for is never two behind
   uint64_t mma_done;
   int kv_bad[kPfStages];  // per stage: bit pp set when page pp of the block is invalid (loaded as zeros)
+  PfTile tiles[kPfMaxTiles];  // this CTA's tiles in walking order, read once from global memory
   uint32_t tmem_base;
   int abort;
 };
 constexpr size_t kPfSmemBytes = sizeof(PfSmem) + 1024;
-
-// One work tile: 32 query tokens of sequence s (from t0) against K/V head g.
-struct PfTile {
-  int s, g, t0, n, q0, ctx, nblocks, npages;
-  bool run;      // has queries and a valid context
-  bool invalid;  // has queries, invalid context: its rows are zeroed
-};
 
 // Tile ti of the grid-wide list: latest token tiles first, then sequence, then K/V head.
 __device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int ti) {
@@ -198,15 +200,20 @@ __device__ __forceinline__ void block_probs(const float (&sv)[64], uint64_t vali
   }
 }
 
-// Persistent: each CTA walks tiles blockIdx.x, + gridDim.x, ...  Every role walks the
-// same list and skips the same tiles, so their running block counters agree; the
-// loader fetches the next tile's Q and K/V while the current one computes, and the
-// MMA warp starts the next tile's S during the current epilogue.
+// Persistent: each CTA walks the tiles blockIdx.x, + gridDim.x, ... (at most kPfMaxTiles;
+// their descriptors are read from global memory once, in parallel, into shared memory).
+// Every role walks the same table and skips the same tiles, so their running block
+// counters agree.  The loader fetches the next tile's Q and block-table entries while the
+// current tile computes; the MMA warp starts the next tile's S during the current one's
+// last blocks; the softmax warps finish a tile (read O, divide, store) only after writing
+// P for the next tile's first block, so the wait for the last P V overlaps useful work.
 __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   PfSmem &sm = *reinterpret_cast<PfSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nt = (a.num_tiles - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);  // <= kPfMaxTiles
 
+  if (tid < nt) sm.tiles[tid] = pf_tile(a, int(blockIdx.x) + tid * int(gridDim.x));
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 32);
@@ -240,47 +247,57 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // index of the first running tile at or after k
+  auto next_run = [&](int k) {
+    while (k < nt && !sm.tiles[k].run) ++k;
+    return k;
+  };
 
   if (warp == 4) {
-    // ================= loader: Q rows (plain loads) and K/V blocks (tiled TMA) =================
+    // ================= loader: Q rows (cp.async) and K/V blocks (tiled TMA) =================
     const uint64_t policy = policy_evict_last();
     if (lane == 0) {
       prefetch_tensormap(&a.tmap_k);
       prefetch_tensormap(&a.tmap_v);
     }
-    long long gb = 0;  // K/V blocks issued so far
-    int lt = 0;        // tiles run so far
-    bool ok = true;
-    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
-      const PfTile t = pf_tile(a, ti);
-      if (!t.run) continue;
+    // block-table entries of a tile's first 128 pages: page lp sits in lane lp % 32, slot lp / 32
+    auto load_entries = [&](const PfTile &t, int (&e)[4]) {
       const int32_t *table = a.block_tables + (long long)t.s * a.bt_stride;
-      // block-table entries of the first 128 pages: page lp sits in lane lp % 32, slot lp / 32
-      int ent[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int lp = lane + 32 * k;
-        ent[k] = lp < t.npages ? __ldg(table + lp) : -1;
+        e[k] = lp < t.npages ? __ldg(table + lp) : -1;
       }
-      // Q of this tile into buffer lt % 2: lane = 16-byte chunk of a token's 4 head rows
-      // (a padding token past n repeats the last real token; its rows are not written)
-      const int qb = lt & 1;
-      if (lt >= 2) {
-        const bool w = pf_wait(sm, &sm.q_empty[qb], uint32_t(lt / 2 - 1) & 1, a.status);
-        if (!__all_sync(0xffffffffu, w)) break;
-      }
-      {
-        // asynchronous 16-byte copies; q_full counts one arrival per lane once its copies land
-        const int hh = lane >> 3, c = lane & 7;
-        const uint4 *src = a.q + ((long long)t.q0 * kQHeads + t.g * kGroup) * 8 + lane;
+    };
+    // Q of tile t into buffer qb: lane = 16-byte chunk of a token's 4 head rows (a padding
+    // token past n repeats the last real token; its rows are not written); asynchronous
+    // 16-byte copies, q_full counting one arrival per lane once its copies land
+    auto load_q = [&](const PfTile &t, int qb) {
+      const int hh = lane >> 3, c = lane & 7;
+      const uint4 *src = a.q + ((long long)t.q0 * kQHeads + t.g * kGroup) * 8 + lane;
 #pragma unroll 8
-        for (int tok = 0; tok < kPfTok; ++tok) {
-          const int r = 4 * tok + hh;
-          cp_async_16(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4),
-                      src + (long long)min(t.t0 + tok, t.n - 1) * kQHeads * 8);
-        }
-        cp_async_arrive(&sm.q_full[qb]);
+      for (int tok = 0; tok < kPfTok; ++tok) {
+        const int r = 4 * tok + hh;
+        cp_async_16(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4),
+                    src + (long long)min(t.t0 + tok, t.n - 1) * kQHeads * 8);
       }
+      cp_async_arrive(&sm.q_full[qb]);
+    };
+    long long gb = 0;  // K/V blocks issued so far
+    int lt = 0;        // running tiles started so far
+    bool ok = true;
+    int k = next_run(0);
+    int ent[4] = {-1, -1, -1, -1};
+    if (k < nt) {
+      load_entries(sm.tiles[k], ent);
+      load_q(sm.tiles[k], 0);
+    }
+    while (ok && k < nt) {
+      const PfTile t = sm.tiles[k];
+      const int kn = next_run(k + 1);
+      int ent_next[4] = {-1, -1, -1, -1};
+      if (kn < nt) load_entries(sm.tiles[kn], ent_next);  // in flight while this tile's blocks go out
+      const int32_t *table = a.block_tables + (long long)t.s * a.bt_stride;
       for (int j = 0; j < t.nblocks; ++j, ++gb) {
         const int st = int(gb % kPfStages);
         if (gb >= kPfStages) {
@@ -296,8 +313,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
           const int lp = j * kPfPagesPerBlock + pp;
           int e;
           if (lp < 128) {
-            const int k = lp >> 5;
-            e = __shfl_sync(0xffffffffu, k == 0 ? ent[0] : k == 1 ? ent[1] : k == 2 ? ent[2] : ent[3], lp & 31);
+            const int q = lp >> 5;
+            e = __shfl_sync(0xffffffffu, q == 0 ? ent[0] : q == 1 ? ent[1] : q == 2 ? ent[2] : ent[3], lp & 31);
           } else {
             e = lp < t.npages ? __ldg(table + lp) : -1;
           }
@@ -320,7 +337,22 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
           }
         }
         __syncwarp();
+        if (j == min(1, t.nblocks - 1) && kn < nt) {
+          // the next tile's Q, once the tile before this one released its buffer
+          const int qb = (lt + 1) & 1;
+          if (lt + 1 >= 2) {
+            const bool w = pf_wait(sm, &sm.q_empty[qb], uint32_t((lt + 1) / 2 - 1) & 1, a.status);
+            if (!__all_sync(0xffffffffu, w)) {
+              ok = false;
+              break;
+            }
+          }
+          load_q(sm.tiles[kn], qb);
+        }
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ent[q] = ent_next[q];
+      k = kn;
       ++lt;
     }
     // every copy issued has landed before the CTA exits
@@ -359,9 +391,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       pend = -1;
       return true;
     };
-    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
-      const PfTile t = pf_tile(a, ti);
-      if (!t.run) continue;
+    for (int k = next_run(0); ok && k < nt; k = next_run(k + 1)) {
+      const PfTile t = sm.tiles[k];
       const int qb = lt & 1;
       bool w = pf_wait(sm, &sm.q_full[qb], uint32_t(lt / 2) & 1, a.status);
       if (!__all_sync(0xffffffffu, w)) break;
@@ -424,15 +455,53 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
     const uint32_t lane_base = tmem + (uint32_t(32 * warp) << 16);
     long long gb = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ok && ti < a.num_tiles; ti += gridDim.x) {
-      const PfTile t = pf_tile(a, ti);
+    // the tile whose O is still to be read, divided and stored
+    bool fin = false;
+    int fin_q0 = 0, fin_t0 = 0, fin_n = 0, fin_g = 0;
+    auto finish = [&]() {
+      // wait for the tile's last P V (global block gb - 1); O, and its row-sum column, are final
+      const bool w = pf_wait(sm, &sm.p_free[(gb - 1) & 1], uint32_t((gb - 1) >> 1) & 1, a.status);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after();
+      const float l_sum = __uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim));
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      float *dst = a.out + ((long long)(fin_q0 + fin_t0 + tok) * kQHeads + fin_g * kGroup + hh) * kHeadDim;
+      const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + 32 * half, o);
+        if (fin_t0 + tok < fin_n) {
+          if (wide) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              const float v[8] = {__uint_as_float(o[c]) * inv,     __uint_as_float(o[c + 1]) * inv,
+                                  __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv,
+                                  __uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv,
+                                  __uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv};
+              st_global_v8(dst + 32 * half + c, v);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4 *>(dst + 32 * half + c) =
+                  make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                              __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+          }
+        }
+      }
+      fin = false;
+      return true;
+    };
+    for (int k = 0; ok && k < nt; ++k) {
+      const PfTile t = sm.tiles[k];
       if (t.invalid) {
         // invalid sequence: zero this tile's rows (its tokens, query heads 4g .. 4g+3)
         if (t.t0 == 0 && t.g == 0 && tid == 0) report(a.status, PKV_DEV_BAD_CONTEXT);
         const int rows = min(kPfTok, t.n - t.t0) * kGroup * kHeadDim;
-        for (int k = tid; k < rows; k += kPfRows)
-          a.out[((long long)(t.q0 + t.t0 + k / (kGroup * kHeadDim)) * kQHeads + t.g * kGroup) * kHeadDim +
-                k % (kGroup * kHeadDim)] = 0.f;
+        for (int i = tid; i < rows; i += kPfRows)
+          a.out[((long long)(t.q0 + t.t0 + i / (kGroup * kHeadDim)) * kQHeads + t.g * kGroup) * kHeadDim +
+                i % (kGroup * kHeadDim)] = 0.f;
         continue;
       }
       if (!t.run) continue;
@@ -494,6 +563,10 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         // that last read this buffer finished before S was written)
         tmem_st32(lane_base + kColS + b * kPfKeys, hi);
         tmem_st32(lane_base + kColS + b * kPfKeys + 32, lo);
+        if (j == 0 && fin && !finish()) {  // the previous tile's P V is done once this P is out
+          ok = false;
+          break;
+        }
         if (j >= 1 && __any_sync(0xffffffffu, move)) {
           // a row's reference max moved: once the previous block's P V is done, rescale
           // its O and row sum (before a tile's first block there is nothing to rescale)
@@ -514,43 +587,17 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
           tmem_st1(lane_base + kColO + kHeadDim,
                    __float_as_uint(__uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim)) * alpha));
         }
-        tc_fence_before();
+        tc_fence_before();  // the reads of O above precede this tile's first P V (ordered by p_full)
         mbar_arrive(&sm.p_full[b]);
       }
       if (!ok) break;
-      // ---- epilogue: O / l for the rows of real query tokens ----
-      const bool w = pf_wait(sm, &sm.p_free[(gb - 1) & 1], uint32_t((gb - 1) >> 1) & 1, a.status);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();
-      const float l_sum = __uint_as_float(tmem_ld1(lane_base + kColO + kHeadDim));
-      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      float *dst = a.out + ((long long)(t.q0 + t.t0 + tok) * kQHeads + t.g * kGroup + hh) * kHeadDim;
-      const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * half, o);
-        if (t.t0 + tok < t.n) {
-          if (wide) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              const float v[8] = {__uint_as_float(o[c]) * inv,     __uint_as_float(o[c + 1]) * inv,
-                                  __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv,
-                                  __uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv,
-                                  __uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv};
-              st_global_v8(dst + 32 * half + c, v);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4 *>(dst + 32 * half + c) =
-                  make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                              __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
-          }
-        }
-      }
-      tc_fence_before();  // the reads of O precede the next tile's first P V (ordered by p_full)
+      fin = true;
+      fin_q0 = t.q0;
+      fin_t0 = t.t0;
+      fin_n = t.n;
+      fin_g = t.g;
     }
+    if (ok && fin) finish();
   }
   tc_fence_before();
   __syncthreads();
@@ -612,7 +659,9 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   a.num_tiles = int((long long)num_seqs * tiles * pkv::kKvHeads);
   const int sms = pkv::device_sm_count();
   const int resident = (sms > 0 ? sms : 148) * pkv::kPfCtasPerSm;
-  const unsigned grid = unsigned(a.num_tiles < resident ? a.num_tiles : resident);
+  const int by_table = (a.num_tiles + pkv::kPfMaxTiles - 1) / pkv::kPfMaxTiles;  // tiles per CTA <= kPfMaxTiles
+  const int g = resident > by_table ? resident : by_table;
+  const unsigned grid = unsigned(a.num_tiles < g ? a.num_tiles : g);
   pkv::paged_prefill_kernel<<<grid, pkv::kPfThreads, pkv::kPfSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
