@@ -84,10 +84,10 @@ def test_status_strings(binding):
 
 
 def test_workspace_size_formula(binding):
-    # (max CTAs + num_seqs) slots of 32 heads x (64 acc + (m, l)) floats + 8 ticket counters
+    # (max CTAs + num_seqs) slots of 32 heads x (64 acc + (m, l)) floats + 2 x 8 ticket counters
     n = 256
     slots = binding.decode_max_ctas() + n
-    assert binding.decode_workspace_bytes(n) == slots * (32 * 64 * 4 + 32 * 8 + 8 * 4)
+    assert binding.decode_workspace_bytes(n) == slots * (32 * 64 * 4 + 32 * 8 + 2 * 8 * 4)
 
 
 def test_plan_without_gpu_is_bounded(binding):
