@@ -205,6 +205,8 @@ int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, 
  *   out            device; float32 [total][num_q_heads][head_dim], total = query_start[num_seqs],
  *                  16-byte aligned.
  *   q              device; bf16 [total][num_q_heads][head_dim], 16-byte aligned.
+ *   num_q_rows     rows of q and out (>= total); the kernel reads and writes no row at or
+ *                  past it (a sequence whose query rows would reach past it counts as invalid).
  *   query_start    device; int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
  *   block_tables, block_table_stride, context_lens, max_context: as for decode.
  *   max_query      host bound on every n_s (sizes the grid; longer runs are not computed).
@@ -216,7 +218,7 @@ int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, 
  * K/V read through the block table as in "Distributing K/V into paged blocks".
  */
 int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
-                                const int32_t *query_start, const int32_t *block_tables,
+                                int num_q_rows, const int32_t *query_start, const int32_t *block_tables,
                                 int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
                                 int max_query, int max_context, float scale, int32_t *device_status,
                                 void *stream);

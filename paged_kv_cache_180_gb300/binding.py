@@ -75,7 +75,7 @@ EXPORTS = {
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_paged_decode_attention_noalloc": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _P]),
     "pkv_decode_step": (_I, [_PP, _P, _P, _P, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, _P]),
-    "pkv_paged_prefill_attention": (_I, [_PP, _P, _P, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, _P]),
+    "pkv_paged_prefill_attention": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, _P]),
     "pkv_sched_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
     "pkv_sched_submit": (_I, [_P, _L, _I, _I]),
@@ -224,7 +224,8 @@ def paged_prefill_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.
     """Causal attention of the last n_s cached tokens of each sequence (rows query_start[s] ..)."""
     desc = pool.desc if isinstance(pool, KVPool) else pool
     num_seqs = int(context_lens.shape[0])
-    rc = _lib.pkv_paged_prefill_attention(ctypes.byref(desc), _ptr(out), _ptr(q), int(q.shape[1]), _ptr(query_start),
+    rows = min(int(q.shape[0]), int(out.shape[0]))
+    rc = _lib.pkv_paged_prefill_attention(ctypes.byref(desc), _ptr(out), _ptr(q), int(q.shape[1]), rows, _ptr(query_start),
                                           _ptr(block_tables), block_table_stride, _ptr(context_lens), num_seqs,
                                           max_query, max_context, scale, _ptr(status), _stream(stream))
     _check("pkv_paged_prefill_attention", rc)

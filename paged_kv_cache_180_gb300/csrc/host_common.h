@@ -35,4 +35,9 @@ int device_sm_count();
 // 128-byte rows of one page (128B swizzle); cached per pool.  PKV_OK or an error.
 int pool_tensor_maps(const pkv_pool *pool, int box_rows, CUtensorMap *tk, CUtensorMap *tv);
 
+// TMA tensor map of queries q[rows][num_q_heads][head_dim] (bf16) for boxes of
+// head_dim x box_heads x box_rows, 128-byte swizzled; cached.  PKV_OK or an error.
+int query_tensor_map(const void *q, int rows, int num_q_heads, int head_dim, int box_heads, int box_rows,
+                     CUtensorMap *map);
+
 }  // namespace pkv

@@ -97,17 +97,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
       : "memory");
 }
 
-// ---- cp.async: 16-byte global -> shared copies, completion signalled on an mbarrier ----
-__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
-}
-
-// One arrival on the mbarrier (counted in its expected arrivals) once all of this
-// thread's earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // ---- tiled (tensor) TMA load of a 3-D box, completion counted on an mbarrier ----
 // The x coordinate is always 0 here (whole 128-byte rows), so it is 16-byte aligned.
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,

@@ -25,10 +25,10 @@
 //    so O's column 64 accumulates the row sum of exactly the weights used.
 //  * Warp roles: warps 0-3 own one row each per thread (TMEM lane = row): they read
 //    S, mask, keep the row's reference maximum, write P, and finally read O, divide
-//    and store.  Warp 4 loads: the next tile's Q rows by cp.async (two Q buffers)
-//    and head g's K and V rows of each page by tiled TMA (2 KiB boxes) into a
-//    4-stage ring; pages past the query span come from a coordinate outside the
-//    pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and issues
+//    and store.  Warp 4 loads by tiled TMA: the next tile's Q (one 16 KiB box of 32
+//    query rows x 4 heads; two Q buffers) and head g's K and V rows of each page
+//    (2 KiB boxes) into a 4-stage ring; pages past the query span come from a
+//    coordinate outside the pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and issues
 //    the MMAs from one thread (S of block j, then P V of block j - 1), completion
 //    signalled by tcgen05.commit.
 //  * Online softmax in the exp2 domain with a lazily moved maximum: a row's
@@ -80,14 +80,15 @@ constexpr uint32_t kIdescPV = idesc_bf16(kPfRows, kPvN, true);  // B = [V | ones
 struct PrefillArgs {
   CUtensorMap tmap_k;  // boxes of one head's 16 rows of one page
   CUtensorMap tmap_v;
+  CUtensorMap tmap_q;  // boxes of 32 query rows x one group's 4 heads (rows past num_q_rows read as zeros)
   int num_pages;
-  const uint4 *q;  // [total][32][64] bf16, 8 uint4 per head row
   float *out;      // [total][32][64]
   const int32_t *query_start;
   const int32_t *block_tables;
   long long bt_stride;
   const int32_t *context_lens;
   int num_seqs;
+  int num_q_rows;
   int max_context;
   int tiles_per_seq;
   int num_tiles;  // num_seqs * tiles_per_seq * 8
@@ -139,7 +140,7 @@ __device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int ti) {
   t.n = __ldg(a.query_start + t.s + 1) - t.q0;
   t.ctx = __ldg(a.context_lens + t.s);
   const bool has = t.n > 0 && t.t0 < t.n;
-  t.invalid = has && (t.ctx < 0 || t.ctx > a.max_context || t.n > t.ctx);
+  t.invalid = has && (t.ctx < 0 || t.ctx > a.max_context || t.n > t.ctx || t.q0 < 0 || t.q0 + t.n > a.num_q_rows);
   t.run = has && !t.invalid;
   const int last_pos = t.run ? t.ctx - t.n + min(t.t0 + kPfTok, t.n) - 1 : 0;
   t.nblocks = last_pos / kPfKeys + 1;
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
   if (tid < nt) sm.tiles[tid] = pf_tile(a, int(blockIdx.x) + tid * int(gridDim.x));
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.q_full[i], 32);
+      mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 1);
@@ -254,11 +255,13 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
   };
 
   if (warp == 4) {
-    // ================= loader: Q rows (cp.async) and K/V blocks (tiled TMA) =================
+    // ================= loader: Q tiles and K/V blocks (tiled TMA) =================
     const uint64_t policy = policy_evict_last();
+    const uint64_t policy_q = policy_evict_first();  // each query row is read by one tile
     if (lane == 0) {
       prefetch_tensormap(&a.tmap_k);
       prefetch_tensormap(&a.tmap_v);
+      prefetch_tensormap(&a.tmap_q);
     }
     // block-table entries of a tile's first 128 pages: page lp sits in lane lp % 32, slot lp / 32
     auto load_entries = [&](const PfTile &t, int (&e)[4]) {
@@ -269,19 +272,15 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         e[k] = lp < t.npages ? __ldg(table + lp) : -1;
       }
     };
-    // Q of tile t into buffer qb: lane = 16-byte chunk of a token's 4 head rows (a padding
-    // token past n repeats the last real token; its rows are not written); asynchronous
-    // 16-byte copies, q_full counting one arrival per lane once its copies land
+    // Q of tile t into buffer qb: one tiled TMA box of 32 query rows x the group's 4 heads,
+    // landing as rows 4 * token + head, 128-byte swizzled (rows past num_q_rows read as zeros;
+    // padding rows past n are the next sequence's queries: computed, never written)
     auto load_q = [&](const PfTile &t, int qb) {
-      const int hh = lane >> 3, c = lane & 7;
-      const uint4 *src = a.q + ((long long)t.q0 * kQHeads + t.g * kGroup) * 8 + lane;
-#pragma unroll 8
-      for (int tok = 0; tok < kPfTok; ++tok) {
-        const int r = 4 * tok + hh;
-        cp_async_16(sm.q[qb] + r * kRowBytes + ((c ^ (r & 7)) << 4),
-                    src + (long long)min(t.t0 + tok, t.n - 1) * kQHeads * 8);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.q_full[qb], kPfRows * kRowBytes);
+        tma_load_3d(sm.q[qb], &a.tmap_q, 0, t.g * kGroup, t.q0 + t.t0, &sm.q_full[qb], policy_q);
       }
-      cp_async_arrive(&sm.q_full[qb]);
+      __syncwarp();
     };
     long long gb = 0;  // K/V blocks issued so far
     int lt = 0;        // running tiles started so far
@@ -396,7 +395,6 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       const int qb = lt & 1;
       bool w = pf_wait(sm, &sm.q_full[qb], uint32_t(lt / 2) & 1, a.status);
       if (!__all_sync(0xffffffffu, w)) break;
-      fence_proxy_async_smem();  // Q landed through the generic proxy; the MMAs read it through the async one
       const uint32_t q_base = smem_addr(sm.q[qb]);
       for (int j = 0; j < t.nblocks; ++j, ++gb) {
         const int st = int(gb % kPfStages), b = int(gb & 1);
@@ -499,9 +497,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         // invalid sequence: zero this tile's rows (its tokens, query heads 4g .. 4g+3)
         if (t.t0 == 0 && t.g == 0 && tid == 0) report(a.status, PKV_DEV_BAD_CONTEXT);
         const int rows = min(kPfTok, t.n - t.t0) * kGroup * kHeadDim;
-        for (int i = tid; i < rows; i += kPfRows)
-          a.out[((long long)(t.q0 + t.t0 + i / (kGroup * kHeadDim)) * kQHeads + t.g * kGroup) * kHeadDim +
-                i % (kGroup * kHeadDim)] = 0.f;
+        for (int i = tid; i < rows; i += kPfRows) {
+          const long long row = (long long)t.q0 + t.t0 + i / (kGroup * kHeadDim);
+          if (row >= 0 && row < a.num_q_rows)
+            a.out[(row * kQHeads + t.g * kGroup) * kHeadDim + i % (kGroup * kHeadDim)] = 0.f;
+        }
         continue;
       }
       if (!t.run) continue;
@@ -620,15 +620,16 @@ int setup_prefill_attributes() {
 }  // namespace pkv
 
 extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
-                                           const int32_t *query_start, const int32_t *block_tables,
+                                           int num_q_rows, const int32_t *query_start, const int32_t *block_tables,
                                            int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
                                            int max_query, int max_context, float scale, int32_t *device_status,
                                            void *stream) {
   int rc = pkv::check_pool(pool);
   if (rc != PKV_OK) return rc;
   if (num_q_heads != pkv::kQHeads) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs < 0 || max_query < 0 || max_context < 0 || block_table_stride < 0) return PKV_ERR_SHAPE;
-  if (num_seqs == 0 || max_query == 0) return PKV_OK;
+  if (num_seqs < 0 || max_query < 0 || max_context < 0 || block_table_stride < 0 || num_q_rows < 0)
+    return PKV_ERR_SHAPE;
+  if (num_seqs == 0 || max_query == 0 || num_q_rows == 0) return PKV_OK;
   if (out == nullptr || q == nullptr || query_start == nullptr || block_tables == nullptr || context_lens == nullptr)
     return PKV_ERR_NULL;
   if (!isfinite(scale)) return PKV_ERR_SCALE;
@@ -642,8 +643,10 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   pkv::PrefillArgs a;
   rc = pkv::pool_tensor_maps(pool, pkv::kPageTokens, &a.tmap_k, &a.tmap_v);
   if (rc != PKV_OK) return rc;
+  rc = pkv::query_tensor_map(q, num_q_rows, pkv::kQHeads, pkv::kHeadDim, pkv::kGroup, pkv::kPfTok, &a.tmap_q);
+  if (rc != PKV_OK) return rc;
   a.num_pages = pool->num_pages;
-  a.q = static_cast<const uint4 *>(q);
+  a.num_q_rows = num_q_rows;
   a.out = out;
   a.query_start = query_start;
   a.block_tables = block_tables;

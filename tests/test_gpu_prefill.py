@@ -117,3 +117,28 @@ def test_invalid_page_inside_a_span():
     assert st & 4 and err & 4
     assert np.isfinite(got[qs[0]:qs[1]]).all()
     U.assert_close(got[qs[1]:qs[2]], ref[qs[1]:qs[2]], "sequence beside the invalid page")
+
+
+def test_query_rows_past_the_buffers():
+    # q and out one row shorter than query_start says: the last sequence counts as invalid
+    # (status bit, nothing read or written past the buffers); the other one is exact
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.custom(609, [300, 70], name="short_rows")
+    nq = [100, 40]
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    qs = np.array([0, 100, 140], dtype=np.int32)
+    qbits = rng.normal_bf16(rng.stream_key(2, "pf-q"), 0, 140 * 32 * 64).reshape(140, 32, 64)
+    q = U.to_dev(qbits)[:139]
+    out = torch.full((139, 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
+    bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    pkv.paged_prefill_attention(d.pool, out, q, U.to_dev(qs), U.to_dev(bt_host), bt_host.shape[1], d.lens, 100,
+                                wl.max_context, wl.scale, d.status)
+    got = out.cpu().double().numpy()
+    assert d.status_value() & 2
+    opool = oracle.Pool(wl.num_pages)
+    k, v, slots = wl.kv_all(0)
+    oracle.kv_append(opool, k, v, slots)
+    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    U.assert_close(got[:100], ref[:100], "sequence inside the buffers")
+    assert not got[100:].any()
