@@ -28,9 +28,9 @@
 //    and store.  Warp 4 loads by tiled TMA: the next tile's Q (one 16 KiB box of 32
 //    query rows x 4 heads; two Q buffers) and head g's K and V rows of each page
 //    (2 KiB boxes) into a 4-stage ring; pages past the query span come from a
-//    coordinate outside the pool, which TMA fills with zeros.  Warp 5 owns the TMEM allocation and issues
-//    the MMAs from one thread (S of block j, then P V of block j - 1), completion
-//    signalled by tcgen05.commit.
+//    coordinate outside the pool, which TMA fills with zeros.  Warp 5 owns the TMEM
+//    allocation and issues the MMAs from one thread (S of block j, then P V of block
+//    j - 1), completion signalled by tcgen05.commit.
 //  * Online softmax in the exp2 domain with a lazily moved maximum: a row's
 //    reference moves only when a block's maximum exceeds it by more than 8 (a
 //    factor 256), and only then is the row of O (with its sum column) rescaled in
