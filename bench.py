@@ -433,35 +433,59 @@ def run_native(args):
     # ---- end to end through the public calls with host buffers ----
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        h_q = [pin(x) for x in q]
-        h_dec = [tuple(pin(x) for x in d) for d in dec]
-        h_bt, h_lens = pin(bt), pin(lens)
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q = [torch.empty_like(x) for x in q]
-        d_dec = [tuple(torch.empty_like(x) for x in d) for d in dec]
-        d_bt, d_lens = torch.empty_like(bt), torch.empty_like(lens)
-        h2d = sum(x.numel() * x.element_size() for x in h_q) + sum(
-            x.numel() * x.element_size() for d in h_dec for x in d) + h_bt.numel() * 4 + h_lens.numel() * 4
-        d2h = h_out.numel() * 4 * L
+        # every input of a step (tables, lengths, and per layer q, new K/V rows, slots) sits
+        # in one pinned host buffer and goes over in one copy; the device tensors are views
+        # of one device buffer
+        parts = [bt, lens] + [x for layer in range(L) for x in (q[layer], *dec[layer])]
+        offs, total = [], 0
+        for x in parts:
+            offs.append(total)
+            total += (x.numel() * x.element_size() + 255) // 256 * 256
+        h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        d_in = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = []
+        for x, o in zip(parts, offs):
+            nb = x.numel() * x.element_size()
+            h_in[o:o + nb].view(x.dtype).view(x.shape).copy_(x.cpu())
+            views.append(d_in[o:o + nb].view(x.dtype).view(x.shape))
+        d_bt, d_lens = views[0], views[1]
+        d_q = [views[2 + 4 * layer] for layer in range(L)]
+        d_dec = [tuple(views[3 + 4 * layer:6 + 4 * layer]) for layer in range(L)]
+        # each layer's output goes to its own slice of one device buffer, read back in one copy
+        d_out = torch.empty((L,) + tuple(out.shape), dtype=out.dtype, device=dev)
+        h_out = torch.empty(d_out.shape, dtype=out.dtype).pin_memory()
+        h2d = total
+        d2h = h_out.numel() * 4
 
-        def e2e_step():
-            d_bt.copy_(h_bt, non_blocking=True)
-            d_lens.copy_(h_lens, non_blocking=True)
+        def e2e_body():
+            d_in.copy_(h_in, non_blocking=True)
             for layer in range(L):
-                d_q[layer].copy_(h_q[layer], non_blocking=True)
-                for dst, src in zip(d_dec[layer], h_dec[layer]):
-                    dst.copy_(src, non_blocking=True)
                 kn, vn, sn = d_dec[layer]
                 bt_l = d_bt.view(-1)[layer * blocks:]
                 if fused:
-                    pkv.decode_step(pool, kn, vn, sn, out, d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                    pkv.decode_step(pool, kn, vn, sn, d_out[layer], d_q[layer], bt_l, stride, d_lens, wl.max_context,
                                     wl.scale, ws, status)
                 else:
                     pkv.kv_append(pool, kn, vn, sn, status)
-                    pkv.paged_decode_attention(pool, out, d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                    pkv.paged_decode_attention(pool, d_out[layer], d_q[layer], bt_l, stride, d_lens, wl.max_context,
                                                wl.scale, ws, status, num_ctas=args.ctas)
-                h_out.copy_(out, non_blocking=True)
+            h_out.copy_(d_out, non_blocking=True)
+
+        g_e2e = None
+        if graphs is not None:
+            # the same calls, copies included, replayed as one CUDA graph per step
+            e2e_body()
+            torch.cuda.synchronize()
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e):
+                e2e_body()
+            stream = torch.cuda.current_stream(dev)
+
+        def e2e_step():
+            if g_e2e is not None:
+                g_e2e.replay()
+            else:
+                e2e_body()
             stream.synchronize()
 
         e2e_steps = max(3, min(steps, 200))
@@ -479,8 +503,9 @@ def run_native(args):
         e2e = {"value": round(whole_job_gbs(bytes_step, world, t_e2e * 1e3), 3), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(t_e2e * 1e3, 4),
-               "how": "host wall clock per step: pinned H2D of q, new K/V, slots, tables, lengths; append + "
-                      "attention; D2H of the output; stream synchronize"}
+               "how": "host wall clock per step: one pinned H2D copy of q, new K/V, slots, tables, lengths; "
+                      "append + attention per layer; one D2H copy of every layer's output; stream synchronize" +
+                      ("; the step's copies and launches replayed as one CUDA graph" if g_e2e is not None else "")}
 
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
