@@ -284,3 +284,43 @@ def test_decode_step_with_skipped_appends_and_partial_pages():
 
 def test_decode_step_llama_layers():
     _decode_step_case(configs.llama_step(), layers=(0, 7, 15))
+
+
+def test_graph_captured_llama_step_all_layers():
+    """The 16-layer fused step (per-layer block-table slices) captured once as a CUDA graph
+    and replayed twice: every layer's output matches the oracle and the replays leave the
+    pool and the merge counters consistent."""
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+    wl = configs.llama_step()
+    L, blocks = wl.num_layers, wl.max_blocks
+    d = U.DeviceDecode(wl)
+    for layer in range(L):
+        k, v, slots = torch_gen.workload_kv(wl, layer, U.dev(), upto_offset=1)
+        if slots.numel():
+            pkv.kv_append(d.pool, k, v, slots, d.status)
+    dec = [tuple(U.to_dev(a) for a in wl.decode_tokens(layer)) for layer in range(L)]
+    qs = [d.q(layer) for layer in range(L)]
+    outs = torch.empty((L, wl.num_seqs, 32, 64), dtype=torch.float32, device=U.dev())
+
+    def step():
+        for layer in range(L):
+            kn, vn, sn = dec[layer]
+            pkv.decode_step(d.pool, kn, vn, sn, outs[layer], qs[layer], d.bt.view(-1)[layer * blocks:], L * blocks,
+                            d.lens, wl.max_context, wl.scale, d.ws, d.status)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    outs.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert d.status_value() == 0
+    got = outs.cpu().double().numpy()
+    for layer in range(L):
+        ref, err, _ = oracle.decode_workload(wl, layer=layer)
+        assert err == 0
+        U.assert_close(got[layer], ref, f"graph replay, layer {layer}")
