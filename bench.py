@@ -433,59 +433,55 @@ def run_native(args):
     # ---- end to end through the public calls with host buffers ----
     e2e = None
     if not args.no_e2e:
-        # every input of a step (tables, lengths, and per layer q, new K/V rows, slots) sits
-        # in one pinned host buffer and goes over in one copy; the device tensors are views
-        # of one device buffer
+        # Every input of a step (tables, lengths, and per layer q, new K/V rows, slots) sits in
+        # one pinned host buffer, and every layer's output goes to one pinned host buffer.  The
+        # tables and lengths (read once per page) are copied to the device; q, the new rows and
+        # the slots are passed as mapped host pointers and the output is written straight to
+        # host memory, so the kernel itself moves them over the host link.
         parts = [bt, lens] + [x for layer in range(L) for x in (q[layer], *dec[layer])]
         offs, total = [], 0
         for x in parts:
             offs.append(total)
             total += (x.numel() * x.element_size() + 255) // 256 * 256
         h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
-        d_in = torch.empty(total, dtype=torch.uint8, device=dev)
-        views = []
+        copied = offs[2]  # the tables and lengths lead the buffer
+        d_in = torch.empty(copied, dtype=torch.uint8, device=dev)
+        h_views = []
         for x, o in zip(parts, offs):
             nb = x.numel() * x.element_size()
-            h_in[o:o + nb].view(x.dtype).view(x.shape).copy_(x.cpu())
-            views.append(d_in[o:o + nb].view(x.dtype).view(x.shape))
-        d_bt, d_lens = views[0], views[1]
-        d_q = [views[2 + 4 * layer] for layer in range(L)]
-        d_dec = [tuple(views[3 + 4 * layer:6 + 4 * layer]) for layer in range(L)]
-        # each layer's output goes to its own slice of one device buffer, read back in one copy
-        d_out = torch.empty((L,) + tuple(out.shape), dtype=out.dtype, device=dev)
-        h_out = torch.empty(d_out.shape, dtype=out.dtype).pin_memory()
+            h_views.append(h_in[o:o + nb].view(x.dtype).view(x.shape))
+            h_views[-1].copy_(x.cpu())
+        d_bt = d_in[offs[0]:offs[0] + bt.numel() * 4].view(torch.int32).view(bt.shape)
+        d_lens = d_in[offs[1]:offs[1] + lens.numel() * 4].view(torch.int32).view(lens.shape)
+        h_q = [h_views[2 + 4 * layer] for layer in range(L)]
+        h_dec = [tuple(h_views[3 + 4 * layer:6 + 4 * layer]) for layer in range(L)]
+        h_out = torch.empty((L,) + tuple(out.shape), dtype=out.dtype).pin_memory()
         h2d = total
         d2h = h_out.numel() * 4
 
         def e2e_body():
-            d_in.copy_(h_in, non_blocking=True)
+            d_in.copy_(h_in[:copied], non_blocking=True)
             for layer in range(L):
-                kn, vn, sn = d_dec[layer]
+                kn, vn, sn = h_dec[layer]
                 bt_l = d_bt.view(-1)[layer * blocks:]
                 if fused:
-                    pkv.decode_step(pool, kn, vn, sn, d_out[layer], d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                    pkv.decode_step(pool, kn, vn, sn, h_out[layer], h_q[layer], bt_l, stride, d_lens, wl.max_context,
                                     wl.scale, ws, status)
                 else:
                     pkv.kv_append(pool, kn, vn, sn, status)
-                    pkv.paged_decode_attention(pool, d_out[layer], d_q[layer], bt_l, stride, d_lens, wl.max_context,
+                    pkv.paged_decode_attention(pool, h_out[layer], h_q[layer], bt_l, stride, d_lens, wl.max_context,
                                                wl.scale, ws, status, num_ctas=args.ctas)
-            h_out.copy_(d_out, non_blocking=True)
 
-        g_e2e = None
-        if graphs is not None:
-            # the same calls, copies included, replayed as one CUDA graph per step
+        # the step's copy and launches are replayed as one CUDA graph
+        e2e_body()
+        torch.cuda.synchronize()
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e):
             e2e_body()
-            torch.cuda.synchronize()
-            g_e2e = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_e2e):
-                e2e_body()
-            stream = torch.cuda.current_stream(dev)
+        stream = torch.cuda.current_stream(dev)
 
         def e2e_step():
-            if g_e2e is not None:
-                g_e2e.replay()
-            else:
-                e2e_body()
+            g_e2e.replay()
             stream.synchronize()
 
         e2e_steps = max(3, min(steps, 200))
@@ -500,12 +496,14 @@ def run_native(args):
             e2e_step()
             ts.append(time.perf_counter() - t0)
         t_e2e = max_over_ranks(sum(ts) / len(ts), dev)
+        # the last layer's output through host memory equals the device-resident run's, bit for bit
+        e2e_same = bool(torch.equal(h_out[L - 1], out.cpu()))
         e2e = {"value": round(whole_job_gbs(bytes_step, world, t_e2e * 1e3), 3), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(t_e2e * 1e3, 4),
-               "how": "host wall clock per step: one pinned H2D copy of q, new K/V, slots, tables, lengths; "
-                      "append + attention per layer; one D2H copy of every layer's output; stream synchronize" +
-                      ("; the step's copies and launches replayed as one CUDA graph" if g_e2e is not None else "")}
+               "ms_per_step": round(t_e2e * 1e3, 4), "matches_device_run": e2e_same,
+               "how": "host wall clock per step, one CUDA graph replay + stream synchronize: H2D copy of the "
+                      "tables and lengths from pinned memory; q, new K/V rows and slots read by the kernel from "
+                      "mapped pinned host memory; every layer's output written to pinned host memory"}
 
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"

@@ -26,7 +26,10 @@
  *  - Buffers are owned by the caller.  The library never allocates, frees or
  *    synchronises; device work is enqueued on the caller's stream.
  *  - "device" pointers must be CUDA device (or managed) memory of the current
- *    device; "host" pointers are ordinary host memory.
+ *    device; "host" pointers are ordinary host memory.  An argument marked
+ *    "device or mapped host" may also be pinned host memory mapped into the device
+ *    address space (cudaHostAlloc, cudaHostRegister): the kernel then reads or writes
+ *    it over the host link (NVLink-C2C on Grace-Blackwell), with no separate copy.
  *  - bf16 values are passed as raw 16-bit patterns (bfloat16, i.e. the upper
  *    half of an IEEE binary32).
  *  - Host-checkable faults return a negative PKV_ERR_* code and enqueue
@@ -111,8 +114,8 @@ int pkv_kv_pool_create(void *k_pool, void *v_pool, int64_t page_stride_bytes, in
 /*
  * pkv_kv_append - scatter the K/V of num_tokens new tokens into their slots (bit copy).
  *   pool          host; descriptor from pkv_kv_pool_create.
- *   k_new, v_new  device; bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned.
- *   slot_mapping  device; int32 [num_tokens]; slot = page * page_tokens + row; a negative slot
+ *   k_new, v_new  device or mapped host; bf16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned.
+ *   slot_mapping  device or mapped host; int32 [num_tokens]; slot = page * page_tokens + row; a negative slot
  *                 is padding and is skipped; a slot >= num_pages * page_tokens is skipped and
  *                 sets PKV_DEV_BAD_SLOT.
  *   device_status device int32, nullable.
@@ -143,8 +146,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim);
  *   row t % page_tokens.
  *
  *   pool               host; descriptor.
- *   out                device; float32 [num_seqs][num_q_heads][head_dim], 8-byte aligned.
- *   q                  device; bf16 [num_seqs][num_q_heads][head_dim], 16-byte aligned.
+ *   out                device or mapped host; float32 [num_seqs][num_q_heads][head_dim], 8-byte aligned.
+ *   q                  device or mapped host; bf16 [num_seqs][num_q_heads][head_dim], 16-byte aligned.
  *   block_tables       device; int32; row s starts at s * block_table_stride and holds at least
  *                      ceil(max_context / page_tokens) entries (a multi-layer table
  *                      [seq][layer][blocks] is passed as base + layer * blocks with
@@ -175,9 +178,9 @@ int pkv_paged_decode_attention(const pkv_pool *pool, float *out, const void *q, 
 /*
  * pkv_decode_step - one decode step for num_seqs sequences in one launch: append each
  * sequence's new token, then attend (pkv_kv_append followed by pkv_paged_decode_attention,
- * fused).  k_new, v_new (device, bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned)
+ * fused).  k_new, v_new (device or mapped host, bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned)
  * hold sequence s's new token, which is position context_lens[s] - 1 (the last token
- * attended); slot_mapping[s] (device int32) is that position's slot in the pool (it must lie
+ * attended); slot_mapping[s] (device or mapped host, int32) is that position's slot in the pool (it must lie
  * in the last page of the sequence's block-table row); a negative slot means sequence s has
  * no new token this step (its cached tokens are attended as they are).  The CTA that holds
  * a sequence's last page takes the new token's rows straight from k_new/v_new and writes
