@@ -324,3 +324,46 @@ def test_graph_captured_llama_step_all_layers():
         ref, err, _ = oracle.decode_workload(wl, layer=layer)
         assert err == 0
         U.assert_close(got[layer], ref, f"graph replay, layer {layer}")
+
+
+def test_decode_step_with_mapped_host_buffers():
+    """q, the new K/V rows and the slots in pinned host memory (read by the kernel over the host
+    link) and the output written straight to pinned host memory: same bits as the device run."""
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+    wl = configs.ragged(seed=492, num_seqs=24)
+    outs = []
+    for mapped in (False, True):
+        d = U.DeviceDecode(wl)
+        k, v, slots = torch_gen.workload_kv(wl, 0, U.dev(), upto_offset=1)
+        if slots.numel():
+            pkv.kv_append(d.pool, k, v, slots, d.status)
+        kn, vn, sn = (U.to_dev(a) for a in wl.decode_tokens(0))
+        q = d.q(0)
+        out = d.out
+        if mapped:
+            kn, vn, sn, q = (x.cpu().pin_memory() for x in (kn, vn, sn, q))
+            out = torch.full(tuple(d.out.shape), float("nan"), dtype=torch.float32).pin_memory()
+        pkv.decode_step(d.pool, kn, vn, sn, out, q, d.bt.view(-1), wl.num_layers * wl.max_blocks, d.lens,
+                        wl.max_context, wl.scale, d.ws, d.status)
+        assert d.status_value() == 0
+        outs.append(out.cpu().clone())
+        if mapped:
+            ref, err, opool = oracle.decode_workload(wl, layer=0)
+            assert err == 0
+            U.assert_close(outs[-1].double().numpy(), ref, "decode_step, mapped host buffers")
+            np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), opool.data.reshape(-1))
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_kv_append_from_mapped_host_buffers():
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.ragged(seed=493, num_seqs=8)
+    d = U.DeviceDecode(wl)
+    k, v, slots = wl.kv_all(0)
+    kh, vh, sh = (U.to_dev(a).cpu().pin_memory() for a in (k, v, slots))
+    pkv.kv_append(d.pool, kh, vh, sh, d.status)
+    assert d.status_value() == 0
+    opool = oracle.Pool(wl.num_pages)
+    oracle.kv_append(opool, k, v, slots)
+    np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), opool.data.reshape(-1))
