@@ -57,6 +57,9 @@ def parse_args():
                         "paged_decode_attention")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step as a CUDA graph (auto: on for the launch-bound workloads)")
+    p.add_argument("--overlap", choices=["auto", "on", "off"], default="auto",
+                   help="launch each layer's fused step with PKV_OVERLAP_PREVIOUS, so it starts while the "
+                        "previous layer's finishes (auto: on for multi-layer fused steps)")
     return p.parse_args()
 
 
@@ -329,6 +332,8 @@ def run_native(args):
             flush_r.max()
 
     fused = args.step == "fused"
+    # the layers' steps read disjoint pages, so each may start while the previous one finishes
+    overlap = fused and (args.overlap == "on" or (args.overlap == "auto" and L > 1))
 
     def step(e_marks=None, attention_only=False):
         for layer in range(L):
@@ -340,7 +345,7 @@ def run_native(args):
                 if e_marks is not None:
                     e_marks[1].record(stream)
                 pkv.decode_step(pool, kn, vn, sn, out, q[layer], bt_l, stride, lens, wl.max_context, wl.scale, ws,
-                                status)
+                                status, overlap_previous=overlap and layer > 0)
             else:
                 if not attention_only:
                     pkv.kv_append(pool, kn, vn, sn, status)
@@ -466,7 +471,7 @@ def run_native(args):
                 bt_l = d_bt.view(-1)[layer * blocks:]
                 if fused:
                     pkv.decode_step(pool, kn, vn, sn, h_out[layer], h_q[layer], bt_l, stride, d_lens, wl.max_context,
-                                    wl.scale, ws, status)
+                                    wl.scale, ws, status, overlap_previous=overlap and layer > 0)
                 else:
                     pkv.kv_append(pool, kn, vn, sn, status)
                     pkv.paged_decode_attention(pool, h_out[layer], h_q[layer], bt_l, stride, d_lens, wl.max_context,
@@ -538,7 +543,7 @@ def run_native(args):
                           else {("kv_append" if graphs is None else "append (step minus attention)"):
                                 round(1e3 * sum(append_ms) / len(append_ms), 3),
                                 "paged_decode_attention": round(1e3 * sum(attn_ms) / len(attn_ms), 3)}),
-            "step_kind": args.step,
+            "step_kind": args.step, "overlap_previous": bool(overlap),
             "clocks": clocks,
             "gpu_launches": steps * L * ((0 if fused else 1) + attn_launches)
                             + (steps * L * attn_launches if graphs is not None else 0),

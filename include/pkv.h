@@ -196,6 +196,27 @@ int pkv_decode_step(const pkv_pool *pool, const void *k_new, const void *v_new, 
                     float scale, void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
 
 /*
+ * pkv_decode_step_ex - pkv_decode_step with launch flags.
+ *   flags   0, or PKV_OVERLAP_PREVIOUS: the kernel is launched with programmatic stream
+ *           serialization, so it may start while the kernel before it on the stream is still
+ *           running.  It then reads context_lens, block_tables and the pool pages it attends
+ *           (and issues their copies) at once, and reads q, k_new, v_new, slot_mapping and
+ *           writes out, the pool, the workspace and device_status only after that kernel has
+ *           completed.  Use it only when the kernel before it on the stream writes none of
+ *           context_lens, block_tables or those pool pages (for example the previous layer's
+ *           step of a multi-layer decode, whose pages differ); inside a CUDA graph capture the
+ *           relation becomes a programmatic edge between the two kernel nodes.
+ *           Other bits return PKV_ERR_SHAPE.
+ * Everything else as pkv_decode_step.
+ */
+#define PKV_OVERLAP_PREVIOUS 1u
+int pkv_decode_step_ex(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                       float *out, const void *q, int num_q_heads, const int32_t *block_tables,
+                       int64_t block_table_stride, const int32_t *context_lens, int num_seqs, int max_context,
+                       float scale, void *workspace, size_t workspace_bytes, int32_t *device_status,
+                       unsigned flags, void *stream);
+
+/*
  * pkv_paged_prefill_attention - causal attention of a chunk of query tokens per sequence
  * over its paged K/V (prefill, chunked prefill; one query per sequence is decode).
  *

@@ -75,6 +75,7 @@ EXPORTS = {
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_paged_decode_attention_noalloc": (_I, [_PP, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _P]),
     "pkv_decode_step": (_I, [_PP, _P, _P, _P, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, _P]),
+    "pkv_decode_step_ex": (_I, [_PP, _P, _P, _P, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, ctypes.c_uint, _P]),
     "pkv_paged_prefill_attention": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, _P]),
     "pkv_sched_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
@@ -84,6 +85,7 @@ EXPORTS = {
 }
 
 NOALLOC_MAX_SEQS = 512  # PKV_NOALLOC_MAX_SEQS
+OVERLAP_PREVIOUS = 1  # PKV_OVERLAP_PREVIOUS
 
 for _name, (_res, _args) in EXPORTS.items():
     _fn = getattr(_lib, _name)
@@ -205,16 +207,19 @@ def paged_decode_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.T
 def decode_step(pool: KVPool | PkvPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                 out: torch.Tensor, q: torch.Tensor, block_tables: torch.Tensor, block_table_stride: int,
                 context_lens: torch.Tensor, max_context: int, scale: float, workspace: torch.Tensor,
-                status: torch.Tensor | None = None, stream=None) -> None:
+                status: torch.Tensor | None = None, stream=None, overlap_previous: bool = False) -> None:
     """kv_append of one new token per sequence (position context_lens[s] - 1) fused with
-    paged_decode_attention, in one launch."""
+    paged_decode_attention, in one launch.  overlap_previous: launch with programmatic stream
+    serialization (PKV_OVERLAP_PREVIOUS; only when the kernel before it on the stream writes
+    none of the lengths, tables or pool pages this step reads)."""
     desc = pool.desc if isinstance(pool, KVPool) else pool
     num_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
     ws_bytes = workspace.numel() * workspace.element_size()
-    rc = _lib.pkv_decode_step(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(out), _ptr(q),
-                              num_q_heads, _ptr(block_tables), block_table_stride, _ptr(context_lens), num_seqs,
-                              max_context, scale, _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
-    _check("pkv_decode_step", rc)
+    rc = _lib.pkv_decode_step_ex(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(out),
+                                 _ptr(q), num_q_heads, _ptr(block_tables), block_table_stride, _ptr(context_lens),
+                                 num_seqs, max_context, scale, _ptr(workspace), ws_bytes, _ptr(status),
+                                 OVERLAP_PREVIOUS if overlap_previous else 0, _stream(stream))
+    _check("pkv_decode_step_ex", rc)
 
 
 def paged_prefill_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.Tensor, query_start: torch.Tensor,

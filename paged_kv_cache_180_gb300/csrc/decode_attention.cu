@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
+  // Launched with overlap (PKV_OVERLAP_PREVIOUS), the next kernel may start its own set-up
+  // now; this one reads the lengths, tables and pool pages at once, and q, the new rows and
+  // every global write wait (griddep_wait) until the kernel before it has completed.
+  griddep_launch_dependents();
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -409,15 +413,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   __syncthreads();
   const long long T = sm.total_pages;
   // zero rows of the sequences that have no pages, spread over all launched CTAs
-  for (int s = cta; s < a.num_seqs; s += G) {
-    if (seq_pages(__ldg(a.context_lens + s), a.max_context) == 0) {
-      float4 *row = reinterpret_cast<float4 *>(a.out + (long long)s * kQHeads * kHeadDim);
-      for (int k = tid; k < kQHeads * kHeadDim / 4; k += kThreads) row[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto zero_empty_rows = [&]() {
+    for (int s = cta; s < a.num_seqs; s += G) {
+      if (seq_pages(__ldg(a.context_lens + s), a.max_context) == 0) {
+        float4 *row = reinterpret_cast<float4 *>(a.out + (long long)s * kQHeads * kHeadDim);
+        for (int k = tid; k < kQHeads * kHeadDim / 4; k += kThreads) row[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-  }
+  };
   // The pages are split over Gu <= min(G, T) CTAs, so every CTA below Gu owns at least one page.
   const int Gu = sm.used_ctas;
-  if (cta >= Gu) return;
+  if (cta >= Gu) {
+    griddep_wait();
+    zero_empty_rows();
+    return;
+  }
   const long long pa = (long long)cta * T / Gu, pb = (long long)(cta + 1) * T / Gu;
 
   // ---- first sequence of the range ----
@@ -457,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     if (j + 1 < count) wi.next(a);
   }
   if (tid == 0) atomicMax(&sm.issued, (unsigned long long)first_fill);
+  // the first pages are on their way; what follows reads q and the new rows and writes
+  griddep_wait();
+  zero_empty_rows();
 
   const int quad = lane & 3;     // column pair of the accumulator fragments
   const int hrow = lane >> 2;    // fragment row: query head hrow of the group when < 4
@@ -679,7 +692,8 @@ int setup_kernel_attributes() {
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
            int64_t bt_stride, const int32_t *context_lens, int num_seqs, int max_context, float scale,
            void *workspace, size_t workspace_bytes, int32_t *device_status, int num_ctas, void *stream,
-           const void *k_new = nullptr, const void *v_new = nullptr, const int32_t *slot_mapping = nullptr) {
+           const void *k_new = nullptr, const void *v_new = nullptr, const int32_t *slot_mapping = nullptr,
+           unsigned flags = 0) {
   int rc = check_pool(pool);
   if (rc != PKV_OK) return rc;
   if (num_q_heads != kQHeads) return PKV_ERR_UNSUPPORTED;
@@ -722,6 +736,25 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.num_slots = (long long)pool->num_pages * pool->page_tokens;
   const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (flags & PKV_OVERLAP_PREVIOUS) {
+    // programmatic stream serialization: the kernel may start while the previous kernel on
+    // the stream finishes (see griddep_launch_dependents / griddep_wait in the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_decode_partial_kernel, a) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_LAUNCH;
+    }
+    return PKV_OK;
+  }
   paged_decode_partial_kernel<<<G, kThreads, kSmemBytes, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
   return PKV_OK;
@@ -759,13 +792,24 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const void *k_new, const vo
                                const int32_t *block_tables, int64_t block_table_stride, const int32_t *context_lens,
                                int num_seqs, int max_context, float scale, void *workspace, size_t workspace_bytes,
                                int32_t *device_status, void *stream) {
+  return pkv_decode_step_ex(pool, k_new, v_new, slot_mapping, out, q, num_q_heads, block_tables, block_table_stride,
+                            context_lens, num_seqs, max_context, scale, workspace, workspace_bytes, device_status, 0u,
+                            stream);
+}
+
+extern "C" int pkv_decode_step_ex(const pkv_pool *pool, const void *k_new, const void *v_new,
+                                  const int32_t *slot_mapping, float *out, const void *q, int num_q_heads,
+                                  const int32_t *block_tables, int64_t block_table_stride, const int32_t *context_lens,
+                                  int num_seqs, int max_context, float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t *device_status, unsigned flags, void *stream) {
+  if (flags & ~unsigned(PKV_OVERLAP_PREVIOUS)) return PKV_ERR_SHAPE;
   if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr)) return PKV_ERR_NULL;
   if (num_seqs > 0 && (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) ||
                        (reinterpret_cast<uintptr_t>(slot_mapping) & 3u)))
     return PKV_ERR_ALIGN;
   return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
                      max_context, scale, workspace, workspace_bytes, device_status, 0, stream, k_new, v_new,
-                     slot_mapping);
+                     slot_mapping, flags);
 }
 
 extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out, const void *q, int num_q_heads,

@@ -75,6 +75,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on the stream
+// (launched with programmatic stream serialization) start once every CTA of this grid has
+// issued it; wait blocks until the grids this one depends on have completed and their
+// memory is visible.  Both are no-ops when no such launch relation exists.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy accesses to shared memory before
 // later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -75,6 +75,13 @@ def test_decode_host_checks_return_before_any_launch(binding):
     assert lib.pkv_kv_append(ctypes.byref(d), P(base), P(base), P(base), 0, None, None) == 0
     assert lib.pkv_kv_append(ctypes.byref(d), P(base + 4), P(base), P(base), 1, None, None) == -4
     assert lib.pkv_kv_append(ctypes.byref(d), None, P(base), P(base), 1, None, None) == -1
+    # decode_step_ex: unknown flag bits are refused before anything else; a null new-row
+    # pointer with a known flag is caught by the pointer checks
+    step = lambda flags, k=base: lib.pkv_decode_step_ex(  # noqa: E731
+        ctypes.byref(d), P(k), P(base), P(base), P(base), P(base), 32, P(base), 128, P(base), 4, 2048, 0.125,
+        P(base), ws, None, flags, None)
+    assert step(2) == -2
+    assert step(b.OVERLAP_PREVIOUS, k=0) == -1
 
 
 def test_status_strings(binding):

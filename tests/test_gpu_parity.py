@@ -286,10 +286,14 @@ def test_decode_step_llama_layers():
     _decode_step_case(configs.llama_step(), layers=(0, 7, 15))
 
 
-def test_graph_captured_llama_step_all_layers():
+@pytest.mark.parametrize("overlap", [False, True], ids=["serial", "overlap_previous"])
+def test_graph_captured_llama_step_all_layers(overlap):
     """The 16-layer fused step (per-layer block-table slices) captured once as a CUDA graph
     and replayed twice: every layer's output matches the oracle and the replays leave the
-    pool and the merge counters consistent."""
+    pool and the merge counters consistent.  With overlap_previous each layer's kernel may
+    start (lengths, tables, first page copies) while the previous layer's finishes; the
+    layers share the output buffer and the workspace, which are written only after the
+    previous kernel completed."""
     import paged_kv_cache_180_gb300 as pkv
     from workloads import torch_gen
     wl = configs.llama_step()
@@ -307,7 +311,7 @@ def test_graph_captured_llama_step_all_layers():
         for layer in range(L):
             kn, vn, sn = dec[layer]
             pkv.decode_step(d.pool, kn, vn, sn, outs[layer], qs[layer], d.bt.view(-1)[layer * blocks:], L * blocks,
-                            d.lens, wl.max_context, wl.scale, d.ws, d.status)
+                            d.lens, wl.max_context, wl.scale, d.ws, d.status, overlap_previous=overlap)
 
     step()
     torch.cuda.synchronize()
@@ -367,3 +371,38 @@ def test_kv_append_from_mapped_host_buffers():
     opool = oracle.Pool(wl.num_pages)
     oracle.kv_append(opool, k, v, slots)
     np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), opool.data.reshape(-1))
+
+
+def test_overlapped_steps_sharing_output_and_workspace():
+    """Eager launches with overlap_previous: 16 layers written to ONE output buffer and one
+    workspace, each layer's kernel allowed to start during the previous one's; the buffer
+    ends with the last layer's result, and every layer checked on its own run matches."""
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+    wl = configs.llama_step()
+    L, blocks = wl.num_layers, wl.max_blocks
+    d = U.DeviceDecode(wl)
+    for layer in range(L):
+        k, v, slots = torch_gen.workload_kv(wl, layer, U.dev(), upto_offset=1)
+        if slots.numel():
+            pkv.kv_append(d.pool, k, v, slots, d.status)
+    dec = [tuple(U.to_dev(a) for a in wl.decode_tokens(layer)) for layer in range(L)]
+    qs = [d.q(layer) for layer in range(L)]
+    copies = []
+    for layer in range(L):
+        kn, vn, sn = dec[layer]
+        pkv.decode_step(d.pool, kn, vn, sn, d.out, qs[layer], d.bt.view(-1)[layer * blocks:], L * blocks, d.lens,
+                        wl.max_context, wl.scale, d.ws, d.status, overlap_previous=True)
+        copies.append(d.out.clone())  # a copy kernel between the steps: ordinary stream order
+    assert d.status_value() == 0
+    for layer in (0, 5, 15):
+        ref, err, _ = oracle.decode_workload(wl, layer=layer)
+        assert err == 0
+        U.assert_close(copies[layer].cpu().double().numpy(), ref, f"overlapped eager, layer {layer}")
+    # back to back with no copy in between: the shared output holds the last layer
+    for layer in range(L):
+        kn, vn, sn = dec[layer]
+        pkv.decode_step(d.pool, kn, vn, sn, d.out, qs[layer], d.bt.view(-1)[layer * blocks:], L * blocks, d.lens,
+                        wl.max_context, wl.scale, d.ws, d.status, overlap_previous=True)
+    assert d.status_value() == 0
+    assert torch.equal(d.out, copies[L - 1])
