@@ -102,16 +102,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def committed_traffic():
-    """Per-launch DRAM bytes of the split-context kernel from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
-    src = os.path.join(ROOT, "paged_kv_cache_180_gb300", "csrc", "decode_attention.cu")
+def committed_traffic(record: str, source: str, workload: str):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary (profiles/<record>), if it
+    was taken on the current kernel source (csrc/<source>) and on this workload; else None."""
+    path = os.path.join(ROOT, "profiles", record)
+    src = os.path.join(ROOT, "paged_kv_cache_180_gb300", "csrc", source)
     try:
         with open(path) as f:
             rec = json.load(f)
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec.get("kernel_source_sha256") != sha:
+        if rec.get("kernel_source_sha256") != sha or rec.get("workload_name") != workload:
             return None
         return rec.get("traffic_bytes_per_launch_full_workload")
     except Exception:
@@ -532,7 +532,7 @@ def run_native(args):
             "pct_of_peak": {"measured": round(100 * value / world / peak, 2),
                             "nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
+                         "frac": round(achieved / peak, 4), "traffic": committed_traffic("decode_attention_traffic.json", "decode_attention.cu", wl.name),
                          "kernel": ("pkv_decode_step (append + split-context attention + merge, one launch)"
                                     if (fused and graphs is None) else
                                     "paged_decode_attention (split-context attention + merge, one launch)"),
@@ -807,7 +807,9 @@ def run_prefill(args):
                            "timing": ("CUDA graph replay per step (whole step; attention-only graph for the "
                                       "per-kernel figure)" if graphs is not None else "CUDA events around each kernel")},
                 "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
-                             "frac": round(tflops / peak, 4), "traffic": None,
+                             "frac": round(tflops / peak, 4),
+                             "traffic": committed_traffic("prefill_attention_traffic.json", "prefill_attention.cu",
+                                                          wl.name),
                              "kernel": "paged_prefill_kernel (tcgen05.mma M128 N64, TMEM accumulators, P as bf16 hi + lo)",
                              "algorithmic_flops_per_launch": flops,
                              "avg_launch_us": round(att_s * 1e6, 3),
