@@ -18,21 +18,23 @@ namespace pkv {
 namespace {
 
 constexpr int kChunksPerRow = kRowBytes / 16;                 // 8 x 16 B per (head, token) row
-constexpr int kChunksPerToken = 2 * kKvHeads * kChunksPerRow;  // K and V: 128 chunks
+constexpr int kChunksPerThread = 4;                           // one thread moves half a row (64 B)
+constexpr int kThreadsPerToken = 2 * kKvHeads * kChunksPerRow / kChunksPerThread;  // K and V: 32
 constexpr int kAppendThreads = 256;
 
-// One thread moves one 16-byte chunk: token i, K or V, kv head g, chunk c.
+// One thread moves 4 consecutive 16-byte chunks: token i, K or V, kv head g, half h of the
+// row (the four loads are in flight together).
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     uint8_t *__restrict__ k_base, uint8_t *__restrict__ v_base, long long page_stride, long long num_slots,
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int32_t *__restrict__ slot_mapping,
     int num_tokens, int32_t *status) {
   const long long idx = (long long)blockIdx.x * kAppendThreads + threadIdx.x;
-  const long long token = idx / kChunksPerToken;
+  const long long token = idx / kThreadsPerToken;
   if (token >= num_tokens) return;
-  const int r = int(idx % kChunksPerToken);
-  const int is_v = r / (kKvHeads * kChunksPerRow);
-  const int g = (r / kChunksPerRow) % kKvHeads;
-  const int c = r % kChunksPerRow;
+  const int r = int(idx % kThreadsPerToken);
+  const int is_v = r / (kThreadsPerToken / 2);
+  const int g = (r / 2) % kKvHeads;
+  const int h = r % 2;
   const long long slot = slot_mapping[token];
   if (slot < 0) return;  // padding
   if (slot >= num_slots) {
@@ -41,10 +43,15 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
   }
   const long long page = slot / kPageTokens;
   const int row = int(slot % kPageTokens);
-  const uint4 *src = (is_v ? v_new : k_new) + (token * kKvHeads + g) * kChunksPerRow + c;
-  uint8_t *dst = (is_v ? v_base : k_base) + page * page_stride + (long long)(g * kPageTokens + row) * kRowBytes +
-                 c * 16;
-  *reinterpret_cast<uint4 *>(dst) = __ldg(src);
+  const uint4 *src = (is_v ? v_new : k_new) + (token * kKvHeads + g) * kChunksPerRow + h * kChunksPerThread;
+  uint4 *dst = reinterpret_cast<uint4 *>((is_v ? v_base : k_base) + page * page_stride +
+                                         (long long)(g * kPageTokens + row) * kRowBytes) +
+               h * kChunksPerThread;
+  uint4 x[kChunksPerThread];
+#pragma unroll
+  for (int c = 0; c < kChunksPerThread; ++c) x[c] = __ldg(src + c);
+#pragma unroll
+  for (int c = 0; c < kChunksPerThread; ++c) dst[c] = x[c];
 }
 
 }  // namespace
@@ -59,7 +66,7 @@ extern "C" int pkv_kv_append(const pkv_pool *pool, const void *k_new, const void
   if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
   if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
     return PKV_ERR_ALIGN;
-  const long long threads = (long long)num_tokens * pkv::kChunksPerToken;
+  const long long threads = (long long)num_tokens * pkv::kThreadsPerToken;
   const long long blocks = (threads + pkv::kAppendThreads - 1) / pkv::kAppendThreads;
   if (blocks > 0x7fffffffLL) return PKV_ERR_SHAPE;
   pkv::kv_append_kernel<<<unsigned(blocks), pkv::kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
