@@ -724,13 +724,18 @@ def run_prefill(args):
     flush_r = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def attend():
-        pkv.paged_prefill_attention(pool, out, q, qs, bt, bt.shape[1], lens, plen, wl.max_context, wl.scale, status)
+    # after the append the attention kernel may start its set-up early (it reads the pages only
+    # once the append has completed); alone (attention-only figure) it is launched plainly
+    overlap = args.overlap != "off"
+
+    def attend(after_append=False):
+        pkv.paged_prefill_attention(pool, out, q, qs, bt, bt.shape[1], lens, plen, wl.max_context, wl.scale, status,
+                                    overlap_previous=overlap and after_append)
 
     def step(attention_only=False):
         if not attention_only:
             pkv.kv_append(pool, k, v, slots, status)
-        attend()
+        attend(after_append=not attention_only)
 
     for _ in range(warmup):
         step()
@@ -802,6 +807,7 @@ def run_prefill(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate/out",
                 "data": "synthetic (seeded N(0,1) bf16)",
                 "config": {"workload": "prefill", "num_seqs": nseq, "prompt_tokens": plen, "layers": 1,
+                           "overlap_previous": bool(overlap),
                            "q_heads": 32, "kv_heads": 8, "head_dim": 64, "page_tokens": 16,
                            "l2": "L2 flushed between steps (write of a 2x L2 buffer, then read of another)",
                            "timing": ("CUDA graph replay per step (whole step; attention-only graph for the "

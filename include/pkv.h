@@ -120,6 +120,8 @@ int pkv_kv_pool_create(void *k_pool, void *v_pool, int64_t page_stride_bytes, in
  *                 sets PKV_DEV_BAD_SLOT.
  *   device_status device int32, nullable.
  * Two tokens naming the same slot race (either may win).  num_tokens = 0 enqueues nothing.
+ * A kernel launched right after it with PKV_OVERLAP_PREVIOUS (pkv_decode_step_ex,
+ * pkv_paged_prefill_attention_ex) may begin its set-up while it runs.
  * Cited: samir-vllm README "What works so far" (decode appends one new token at its absolute
  * position); tiny-vllm part 3, "Distributing K/V into paged blocks" (page/row of a token,
  * K and V copied into the block).
@@ -246,6 +248,23 @@ int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, const void *q,
                                 int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
                                 int max_query, int max_context, float scale, int32_t *device_status,
                                 void *stream);
+
+/*
+ * pkv_paged_prefill_attention_ex - pkv_paged_prefill_attention with launch flags.
+ *   flags   0, or PKV_OVERLAP_PREVIOUS: launched with programmatic stream serialization, the
+ *           kernel may start while the kernel before it on the stream is still running; it
+ *           reads query_start, context_lens, block_tables and q at once, and the pool pages
+ *           (and writes out and device_status) only after that kernel has completed.  Use it
+ *           only when the kernel before it writes none of q, query_start, context_lens or
+ *           block_tables - for example pkv_kv_append of the prompt's K/V, which writes only the
+ *           pool.  Other bits return PKV_ERR_SHAPE.
+ * Everything else as pkv_paged_prefill_attention.
+ */
+int pkv_paged_prefill_attention_ex(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                   int num_q_rows, const int32_t *query_start, const int32_t *block_tables,
+                                   int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
+                                   int max_query, int max_context, float scale, int32_t *device_status,
+                                   unsigned flags, void *stream);
 
 /*
  * Same as pkv_paged_decode_attention with the number of CTAs of the split-context pass

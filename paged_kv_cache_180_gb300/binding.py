@@ -77,6 +77,8 @@ EXPORTS = {
     "pkv_decode_step": (_I, [_PP, _P, _P, _P, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, _P]),
     "pkv_decode_step_ex": (_I, [_PP, _P, _P, _P, _P, _P, _I, _P, _L, _P, _I, _I, _F, _P, _Z, _P, ctypes.c_uint, _P]),
     "pkv_paged_prefill_attention": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, _P]),
+    "pkv_paged_prefill_attention_ex": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, ctypes.c_uint,
+                                            _P]),
     "pkv_sched_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
     "pkv_sched_submit": (_I, [_P, _L, _I, _I]),
@@ -225,15 +227,19 @@ def decode_step(pool: KVPool | PkvPool, k_new: torch.Tensor, v_new: torch.Tensor
 def paged_prefill_attention(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.Tensor, query_start: torch.Tensor,
                             block_tables: torch.Tensor, block_table_stride: int, context_lens: torch.Tensor,
                             max_query: int, max_context: int, scale: float, status: torch.Tensor | None = None,
-                            stream=None) -> None:
-    """Causal attention of the last n_s cached tokens of each sequence (rows query_start[s] ..)."""
+                            stream=None, overlap_previous: bool = False) -> None:
+    """Causal attention of the last n_s cached tokens of each sequence (rows query_start[s] ..).
+    overlap_previous: launch with PKV_OVERLAP_PREVIOUS (only when the kernel before it on the
+    stream writes none of q, query_start, context_lens or block_tables, e.g. the prompt's
+    kv_append)."""
     desc = pool.desc if isinstance(pool, KVPool) else pool
     num_seqs = int(context_lens.shape[0])
     rows = min(int(q.shape[0]), int(out.shape[0]))
-    rc = _lib.pkv_paged_prefill_attention(ctypes.byref(desc), _ptr(out), _ptr(q), int(q.shape[1]), rows, _ptr(query_start),
-                                          _ptr(block_tables), block_table_stride, _ptr(context_lens), num_seqs,
-                                          max_query, max_context, scale, _ptr(status), _stream(stream))
-    _check("pkv_paged_prefill_attention", rc)
+    rc = _lib.pkv_paged_prefill_attention_ex(ctypes.byref(desc), _ptr(out), _ptr(q), int(q.shape[1]), rows,
+                                             _ptr(query_start), _ptr(block_tables), block_table_stride,
+                                             _ptr(context_lens), num_seqs, max_query, max_context, scale, _ptr(status),
+                                             OVERLAP_PREVIOUS if overlap_previous else 0, _stream(stream))
+    _check("pkv_paged_prefill_attention_ex", rc)
 
 
 def paged_decode_attention_noalloc(pool: KVPool | PkvPool, out: torch.Tensor, q: torch.Tensor,

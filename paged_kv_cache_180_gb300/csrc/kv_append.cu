@@ -28,6 +28,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
     uint8_t *__restrict__ k_base, uint8_t *__restrict__ v_base, long long page_stride, long long num_slots,
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int32_t *__restrict__ slot_mapping,
     int num_tokens, int32_t *status) {
+  // a kernel launched after this one with PKV_OVERLAP_PREVIOUS may start its set-up now (it
+  // reads the pool only once this kernel has completed)
+  griddep_launch_dependents();
   const long long idx = (long long)blockIdx.x * kAppendThreads + threadIdx.x;
   const long long token = idx / kThreadsPerToken;
   if (token >= num_tokens) return;

@@ -291,6 +291,9 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
       load_entries(sm.tiles[k], ent);
       load_q(sm.tiles[k], 0);
     }
+    // launched with overlap (PKV_OVERLAP_PREVIOUS), the kernel before this one (the append of
+    // the prompt's K/V) may still be running: the pages are read only once it has completed
+    griddep_wait();
     while (ok && k < nt) {
       const PfTile t = sm.tiles[k];
       const int kn = next_run(k + 1);
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
     __syncwarp();
   } else {
     // ================= softmax warps: thread = row = 4 * token + head =================
+    griddep_wait();  // the first global write below comes after the kernel before this one
     const int r = tid, tok = r >> 2, hh = r & 3;
     const uint32_t lane_base = tmem + (uint32_t(32 * warp) << 16);
     long long gb = 0;
@@ -624,6 +628,17 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
                                            int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
                                            int max_query, int max_context, float scale, int32_t *device_status,
                                            void *stream) {
+  return pkv_paged_prefill_attention_ex(pool, out, q, num_q_heads, num_q_rows, query_start, block_tables,
+                                        block_table_stride, context_lens, num_seqs, max_query, max_context, scale,
+                                        device_status, 0u, stream);
+}
+
+extern "C" int pkv_paged_prefill_attention_ex(const pkv_pool *pool, float *out, const void *q, int num_q_heads,
+                                              int num_q_rows, const int32_t *query_start, const int32_t *block_tables,
+                                              int64_t block_table_stride, const int32_t *context_lens, int num_seqs,
+                                              int max_query, int max_context, float scale, int32_t *device_status,
+                                              unsigned flags, void *stream) {
+  if (flags & ~unsigned(PKV_OVERLAP_PREVIOUS)) return PKV_ERR_SHAPE;
   int rc = pkv::check_pool(pool);
   if (rc != PKV_OK) return rc;
   if (num_q_heads != pkv::kQHeads) return PKV_ERR_UNSUPPORTED;
@@ -665,6 +680,25 @@ extern "C" int pkv_paged_prefill_attention(const pkv_pool *pool, float *out, con
   const int by_table = (a.num_tiles + pkv::kPfMaxTiles - 1) / pkv::kPfMaxTiles;  // tiles per CTA <= kPfMaxTiles
   const int g = resident > by_table ? resident : by_table;
   const unsigned grid = unsigned(a.num_tiles < g ? a.num_tiles : g);
+  if (flags & PKV_OVERLAP_PREVIOUS) {
+    // programmatic stream serialization: the set-up (tile table, block-table entries, the first
+    // tile's Q) overlaps the end of the kernel before this one
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(pkv::kPfThreads);
+    cfg.dynamicSmemBytes = pkv::kPfSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, pkv::paged_prefill_kernel, a) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_LAUNCH;
+    }
+    return PKV_OK;
+  }
   pkv::paged_prefill_kernel<<<grid, pkv::kPfThreads, pkv::kPfSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }

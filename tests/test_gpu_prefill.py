@@ -142,3 +142,31 @@ def test_query_rows_past_the_buffers():
     ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
     U.assert_close(got[:100], ref[:100], "sequence inside the buffers")
     assert not got[100:].any()
+
+
+def test_prefill_overlapping_the_append():
+    """The prompt's K/V appended by kv_append into a pool of NaN bytes, and the prefill launched
+    right after it with overlap_previous: its set-up may run during the append, but its page
+    reads come after it (a page read early would bring NaN into the output)."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.custom(612, [512, 300, 1000, 64, 2048], name="overlap")
+    nq = [512, 300, 200, 64, 1]
+    d = U.DeviceDecode(wl)  # pool filled with a NaN pattern
+    k, v, slots = (U.to_dev(a) for a in wl.kv_all(0))
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    total = int(qs[-1])
+    qbits = rng.normal_bf16(rng.stream_key(612, "pf-q"), 0, total * 32 * 64).reshape(total, 32, 64)
+    q, qs_d = U.to_dev(qbits), U.to_dev(qs)
+    bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    bt = U.to_dev(bt_host)
+    out = torch.full((total, 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
+    torch.cuda.synchronize()
+    pkv.kv_append(d.pool, k, v, slots, d.status)
+    pkv.paged_prefill_attention(d.pool, out, q, qs_d, bt, bt_host.shape[1], d.lens, max(nq), wl.max_context,
+                                wl.scale, d.status, overlap_previous=True)
+    assert d.status_value() == 0
+    opool = oracle.Pool(wl.num_pages)
+    oracle.kv_append(opool, *wl.kv_all(0))
+    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    assert err == 0
+    U.assert_close(out.cpu().double().numpy(), ref, "prefill overlapping the append")
