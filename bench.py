@@ -29,6 +29,7 @@ import sys
 import threading
 import time
 from concurrent.futures import ThreadPoolExecutor
+from contextlib import contextmanager
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -57,6 +58,7 @@ def parse_args():
                         "paged_decode_attention")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step as a CUDA graph (auto: on for the launch-bound workloads)")
+    p.add_argument("--nvtx", action="store_true", help="NVTX ranges around the bench phases and steps")
     p.add_argument("--overlap", choices=["auto", "on", "off"], default="auto",
                    help="launch each layer's fused step with PKV_OVERLAP_PREVIOUS, so it starts while the "
                         "previous layer's finishes (auto: on for multi-layer fused steps)")
@@ -100,6 +102,24 @@ def measured_peak():
         return float(peaks["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+NVTX = False  # --nvtx: name the bench phases and steps for a profiler's range filters
+
+
+@contextmanager
+def nvtx(name: str):
+    """An NVTX range around a phase (warm-up, timed steps, end-to-end, CPU baseline) when --nvtx
+    is given, so a capture can be limited to it (ncu --nvtx --nvtx-include "timed/")."""
+    if not NVTX:
+        yield
+        return
+    import torch
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 def committed_traffic(record: str, source: str, workload: str):
@@ -358,9 +378,10 @@ def run_native(args):
                 e_marks = e_marks[3:]
 
     use_graph = args.graph == "on" or (args.graph == "auto" and wl.name != "bandwidth")
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
+    with nvtx("warmup"):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     graphs = None
     if use_graph:
@@ -388,10 +409,12 @@ def run_native(args):
     append_ms, attn_ms, step_ms = [], [], []
     if graphs is None:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
-        for i in range(steps):
-            flush()
-            step(ev[i])
-        torch.cuda.synchronize()
+        with nvtx("timed"):
+            for i in range(steps):
+                flush()
+                with nvtx(f"step {i}"):
+                    step(ev[i])
+            torch.cuda.synchronize()
         for i in range(steps):
             tot = 0.0
             for layer in range(L):
@@ -403,17 +426,19 @@ def run_native(args):
             step_ms.append(tot)
     else:
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * steps)]
-        for i in range(steps):
-            flush()
-            ev[i][0].record(stream)
-            graphs[0].replay()
-            ev[i][1].record(stream)
-        for i in range(steps):
-            flush()
-            ev[steps + i][0].record(stream)
-            graphs[1].replay()
-            ev[steps + i][1].record(stream)
-        torch.cuda.synchronize()
+        with nvtx("timed"):
+            for i in range(steps):
+                flush()
+                ev[i][0].record(stream)
+                graphs[0].replay()
+                ev[i][1].record(stream)
+        with nvtx("timed attention only"):
+            for i in range(steps):
+                flush()
+                ev[steps + i][0].record(stream)
+                graphs[1].replay()
+                ev[steps + i][1].record(stream)
+            torch.cuda.synchronize()
         step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
         attn_ms = [ev[steps + i][0].elapsed_time(ev[steps + i][1]) / L for i in range(steps)]
         append_ms = [max(0.0, step_ms[i] / L - attn_ms[i]) for i in range(steps)]
@@ -493,13 +518,14 @@ def run_native(args):
         for _ in range(3):
             e2e_step()
         ts = []
-        for _ in range(e2e_steps):
-            if flush_w is not None:
-                flush()
-                torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            e2e_step()
-            ts.append(time.perf_counter() - t0)
+        with nvtx("e2e"):
+            for _ in range(e2e_steps):
+                if flush_w is not None:
+                    flush()
+                    torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                e2e_step()
+                ts.append(time.perf_counter() - t0)
         t_e2e = max_over_ranks(sum(ts) / len(ts), dev)
         # the last layer's output through host memory equals the device-resident run's, bit for bit
         e2e_same = bool(torch.equal(h_out[L - 1], out.cpu()))
@@ -555,7 +581,8 @@ def run_native(args):
     # CPU baseline (the oracle as it stands), rank 0 at N=1 only, on the machine's host cores.
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(wl)
+            with nvtx("cpu_baseline"):
+                line["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(line), flush=True)
     return 0
 
@@ -839,7 +866,9 @@ def rng_key(tag: str) -> int:
 
 
 def main():
+    global NVTX
     args = parse_args()
+    NVTX = args.nvtx
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":
