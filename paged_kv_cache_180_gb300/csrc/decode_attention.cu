@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   // Per thread: pages, sequences with pages, and the least and most pages of one sequence.
   long long mine = 0;
   int n_mine = 0, pmin = 0x7fffffff, pmax = 0;
+  bool bad_context = false;  // reported after griddep_wait, like every global write
   for (int i = tid; i < a.num_seqs; i += kThreads) {
     const int c = __ldg(a.context_lens + i);
     const int p = seq_pages(c, a.max_context);
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       pmin = min(pmin, p);
       pmax = max(pmax, p);
     }
-    if (cta == 0 && (c < 0 || c > a.max_context)) report(a.status, PKV_DEV_BAD_CONTEXT);
+    if (cta == 0 && (c < 0 || c > a.max_context)) bad_context = true;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -425,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   const int Gu = sm.used_ctas;
   if (cta >= Gu) {
     griddep_wait();
+    if (bad_context) report(a.status, PKV_DEV_BAD_CONTEXT);
     zero_empty_rows();
     return;
   }
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   if (tid == 0) atomicMax(&sm.issued, (unsigned long long)first_fill);
   // the first pages are on their way; what follows reads q and the new rows and writes
   griddep_wait();
+  if (bad_context) report(a.status, PKV_DEV_BAD_CONTEXT);
   zero_empty_rows();
 
   const int quad = lane & 3;     // column pair of the accumulator fragments
