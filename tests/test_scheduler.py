@@ -129,3 +129,43 @@ def test_stats_hand_example(pkv):
     st = s.stats()
     assert st == dict(pool_pages=8, peak_active=3, largest_batch=3, peak_pages=7, admission_waits=1, free_pages=8,
                       credits_in_use=0, active=0, queued=0, steps=12)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_configurations_match_and_drain(pkv, seed):
+    """Seeded random pools, layer counts, slot counts, context limits and request mixes (some
+    requests too large for the pool, some budgets clamped): the native scheduler matches the
+    reference model at every step, the invariants hold, and every page comes back."""
+    r = np.random.default_rng(9000 + seed)
+    num_pages = int(r.integers(8, 160))
+    num_layers = int(r.integers(1, 4))
+    num_slots = int(r.integers(1, 9))
+    max_context = int(r.choice([64, 256, 2048]))
+    free_order = [int(x) for x in r.permutation(num_pages)] if seed % 2 else None
+    native = pkv.Scheduler(num_pages, num_layers, 16, max_context, num_slots, free_order)
+    model = AdmissionModel(num_pages, num_layers, 16, max_context, num_slots, free_order)
+    accepted = []
+    for rid in range(int(r.integers(3, 16))):
+        p = int(r.integers(1, max_context + 1))
+        n = int(r.integers(1, 80))
+        try:
+            model.submit(rid, p, n)
+        except Rejected:
+            with pytest.raises(pkv.PkvError):
+                native.submit(rid, p, n)
+            continue
+        native.submit(rid, p, n)
+        accepted.append((p, n))
+    work = sum(min(n, max_context - p + 1) for p, n in accepted)
+    plans = []
+    for step in range(work + len(accepted) + 8):
+        a = native.step()
+        b = model.step()
+        for key in ("finished", "admitted", "admitted_slot", "append_request", "append_position", "decode_slot",
+                    "context_lens"):
+            assert list(a[key]) == list(b[key]), (seed, step, key)
+        assert np.array_equal(a["block_tables"], np.array(b["block_tables"], dtype=np.int32)), (seed, step)
+        plans.append(a)
+    _check_invariants(plans, num_pages, num_layers, max_context)
+    st = native.stats()
+    assert st["free_pages"] == num_pages and st["active"] == 0 and st["queued"] == 0 and st["credits_in_use"] == 0
