@@ -82,6 +82,12 @@ def test_decode_host_checks_return_before_any_launch(binding):
         P(base), ws, None, flags, None)
     assert step(2) == -2
     assert step(b.OVERLAP_PREVIOUS, k=0) == -1
+    # prefill_ex: unknown flag bits refused first; a null output with a known flag is caught
+    pre = lambda flags, out=base: lib.pkv_paged_prefill_attention_ex(  # noqa: E731
+        ctypes.byref(d), P(out), P(base), 32, 64, P(base), P(base), 128, P(base), 4, 16, 2048, 0.125, None, flags,
+        None)
+    assert pre(4) == -2
+    assert pre(b.OVERLAP_PREVIOUS, out=0) == -1
 
 
 def test_status_strings(binding):
