@@ -170,3 +170,31 @@ def test_prefill_overlapping_the_append():
     ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
     assert err == 0
     U.assert_close(out.cpu().double().numpy(), ref, "prefill overlapping the append")
+
+
+def test_max_query_bound_leaves_longer_runs_alone():
+    """max_query sizes the grid: only the first max_query query rows of each sequence are
+    computed (exactly); rows past it are not written."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.custom(613, [300, 90, 40], name="maxq")
+    nq = [100, 90, 20]
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    total = int(qs[-1])
+    qbits = rng.normal_bf16(rng.stream_key(613, "pf-q"), 0, total * 32 * 64).reshape(total, 32, 64)
+    out = torch.full((total, 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
+    bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    pkv.paged_prefill_attention(d.pool, out, U.to_dev(qbits), U.to_dev(qs), U.to_dev(bt_host), bt_host.shape[1],
+                                d.lens, 32, wl.max_context, wl.scale, d.status)
+    assert d.status_value() == 0
+    got = out.cpu().double().numpy()
+    opool = oracle.Pool(wl.num_pages)
+    oracle.kv_append(opool, *wl.kv_all(0))
+    ref, err = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    assert err == 0
+    for s in range(3):
+        done = min(nq[s], 32)
+        rows = slice(int(qs[s]), int(qs[s]) + done)
+        U.assert_close(got[rows], ref[rows], f"sequence {s}, first {done} queries")
+        assert np.isnan(got[int(qs[s]) + done:int(qs[s + 1])]).all()
