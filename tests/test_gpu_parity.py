@@ -406,3 +406,48 @@ def test_overlapped_steps_sharing_output_and_workspace():
                         wl.max_context, wl.scale, d.ws, d.status, overlap_previous=True)
     assert d.status_value() == 0
     assert torch.equal(d.out, copies[L - 1])
+
+
+@pytest.mark.parametrize("pad", [0, 256], ids=["packed", "padded_stride"])
+def test_separate_k_and_v_buffers(pad):
+    """K and V pools in two separate allocations with a page stride of half a page (plus
+    optional padding): append bit-exact per half, decode and prefill match the oracle."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.ragged(seed=494, num_seqs=12)
+    half_elems = 8 * 16 * 64
+    stride = half_elems * 2 + pad                       # bytes between pages
+    n_elems = (wl.num_pages * stride) // 2
+    kbuf = torch.full((n_elems,), -1, dtype=torch.int16, device=U.dev()).view(torch.bfloat16)
+    vbuf = torch.full((n_elems,), -1, dtype=torch.int16, device=U.dev()).view(torch.bfloat16)
+    desc = pkv.kv_pool_create(kbuf, vbuf, stride, wl.num_pages)
+    status = torch.zeros(1, dtype=torch.int32, device=U.dev())
+    k, v, slots = wl.kv_all(0)
+    pkv.kv_append(desc, U.to_dev(k), U.to_dev(v), U.to_dev(slots), status)
+    opool = oracle.Pool(wl.num_pages)
+    oracle.kv_append(opool, k, v, slots)
+    for buf, ref_half in ((kbuf, opool.k), (vbuf, opool.v)):
+        pages = U.bits(buf).reshape(wl.num_pages, stride // 2)[:, :half_elems].reshape(ref_half.shape)
+        np.testing.assert_array_equal(pages, ref_half)
+    # decode
+    out = torch.empty(wl.num_seqs, 32, 64, dtype=torch.float32, device=U.dev())
+    ws = pkv.decode_workspace(wl.num_seqs, device=U.dev())
+    bt_host = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    bt, lens = U.to_dev(bt_host), U.to_dev(wl.context_lens)
+    pkv.paged_decode_attention(desc, out, U.to_dev(wl.q(0)), bt, bt_host.shape[1], lens, wl.max_context, wl.scale,
+                               ws, status)
+    assert int(status.item()) == 0
+    ref, err, _ = oracle.decode_workload(wl)
+    assert err == 0
+    U.assert_close(out.cpu().double().numpy(), ref, "decode, separate K and V buffers")
+    # prefill of the last min(ctx, 24) tokens
+    nq = [min(int(c), 24) for c in wl.context_lens]
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    total = int(qs[-1])
+    qbits = rng.normal_bf16(rng.stream_key(494, "pf-q"), 0, total * 32 * 64).reshape(total, 32, 64)
+    pout = torch.full((total, 32, 64), float("nan"), dtype=torch.float32, device=U.dev())
+    pkv.paged_prefill_attention(desc, pout, U.to_dev(qbits), U.to_dev(qs), bt, bt_host.shape[1], lens, max(nq),
+                                wl.max_context, wl.scale, status)
+    assert int(status.item()) == 0
+    pref, perr = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
+    assert perr == 0
+    U.assert_close(pout.cpu().double().numpy(), pref, "prefill, separate K and V buffers")
