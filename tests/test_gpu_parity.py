@@ -451,3 +451,51 @@ def test_separate_k_and_v_buffers(pad):
     pref, perr = oracle.paged_prefill_attention(opool, qbits, qs, bt_host, wl.context_lens, wl.scale, wl.max_context)
     assert perr == 0
     U.assert_close(pout.cpu().double().numpy(), pref, "prefill, separate K and V buffers")
+
+
+def test_calls_run_on_the_callers_stream():
+    """Append and attention enqueued on a side stream (as the current stream, and passed
+    explicitly) are ordered on that stream and match the oracle."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.ragged(seed=495, num_seqs=10)
+    side = torch.cuda.Stream()
+    d = U.DeviceDecode(wl)
+    k, v, slots = (U.to_dev(a) for a in wl.kv_all(0))
+    q = d.q(0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        pkv.kv_append(d.pool, k, v, slots, d.status)  # on the current (side) stream
+    blocks = wl.max_blocks
+    pkv.paged_decode_attention(d.pool, d.out, q, d.bt.view(-1), wl.num_layers * blocks, d.lens, wl.max_context,
+                               wl.scale, d.ws, d.status, stream=side)  # passed explicitly
+    side.synchronize()
+    assert int(d.status.item()) == 0
+    ref, err, _ = oracle.decode_workload(wl)
+    assert err == 0
+    U.assert_close(d.out.cpu().double().numpy(), ref, "side stream")
+
+
+def test_status_word_is_optional():
+    """device_status may be null: calls with no status word (a valid batch, and one with an
+    invalid context that would set a bit) run and give the same rows."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.ragged(seed=496, num_seqs=6)
+    d = U.DeviceDecode(wl)
+    d.append_all()
+    blocks = wl.max_blocks
+    q = d.q(0)
+    pkv.paged_decode_attention(d.pool, d.out, q, d.bt.view(-1), wl.num_layers * blocks, d.lens, wl.max_context,
+                               wl.scale, d.ws, None)
+    torch.cuda.synchronize()
+    ref, err, _ = oracle.decode_workload(wl)
+    assert err == 0
+    U.assert_close(d.out.cpu().double().numpy(), ref, "no status word")
+    bad_lens = d.lens.clone()
+    bad_lens[2] = wl.max_context + 1
+    pkv.paged_decode_attention(d.pool, d.out, q, d.bt.view(-1), wl.num_layers * blocks, bad_lens, wl.max_context,
+                               wl.scale, d.ws, None)
+    torch.cuda.synchronize()
+    got = d.out.cpu().double().numpy()
+    assert np.isfinite(got).all() and not got[2].any()   # the invalid sequence's rows are zeros
+    keep = [s for s in range(wl.num_seqs) if s != 2]
+    U.assert_close(got[keep], ref[keep], "no status word, one invalid context")
