@@ -66,9 +66,11 @@ extern "C" {
 #define PKV_ERR_NO_PAGE (-10)      /* allocator: no free page */
 #define PKV_ERR_STATE (-11)        /* scheduler/allocator used out of order */
 #define PKV_ERR_NOALLOC_LIMIT (-12) /* num_seqs above the fixed scratch of the allocation-free entry point */
+#define PKV_ERR_NO_CREDIT (-13)    /* allocator: a request's credits do not fit beside the admitted ones now */
 
 /* ---- device status bits (OR-ed into *device_status) --------------------- */
-#define PKV_DEV_BAD_SLOT 1u        /* kv_append: slot >= num_pages * page_tokens; token not written */
+#define PKV_DEV_BAD_SLOT 1u        /* kv_append: slot >= num_pages * page_tokens; decode_step: slot is not
+                                      position ctx - 1 of the sequence; the token is not written */
 #define PKV_DEV_BAD_CONTEXT 2u     /* context_lens[s] < 0 or > max_context; row s of out is zeros */
 #define PKV_DEV_BAD_PAGE 4u        /* block-table entry outside [0, num_pages) inside the context;
                                       that page's tokens are left out of the softmax */
@@ -182,13 +184,15 @@ int pkv_paged_decode_attention(const pkv_pool *pool, float *out, const void *q, 
  * sequence's new token, then attend (pkv_kv_append followed by pkv_paged_decode_attention,
  * fused).  k_new, v_new (device or mapped host, bf16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned)
  * hold sequence s's new token, which is position context_lens[s] - 1 (the last token
- * attended); slot_mapping[s] (device or mapped host, int32) is that position's slot in the pool (it must lie
- * in the last page of the sequence's block-table row); a negative slot means sequence s has
- * no new token this step (its cached tokens are attended as they are).  The CTA that holds
- * a sequence's last page takes the new token's rows straight from k_new/v_new and writes
- * them to the pool.  A slot past the pool sets PKV_DEV_BAD_SLOT (the token is still
- * attended, not stored).  A sequence with context 0 appends nothing.  Other arguments,
- * errors and results are those of pkv_paged_decode_attention.
+ * attended); slot_mapping[s] (device or mapped host, int32) is that position's slot in the
+ * pool: block_tables[s][(ctx - 1) / page_tokens] * page_tokens + (ctx - 1) % page_tokens.
+ * A negative slot means sequence s has no new token this step (its cached tokens are
+ * attended as they are).  The CTA that holds a sequence's last page takes the new token's
+ * rows straight from k_new/v_new and writes them to the pool.  Any other non-negative slot
+ * (not that position, or past the pool) sets PKV_DEV_BAD_SLOT: the token is neither stored
+ * nor attended, and the sequence is attended over its cached rows as they are.  A sequence
+ * with context 0 appends nothing.  Other arguments, errors and results are those of
+ * pkv_paged_decode_attention.
  * Cited: samir-vllm README "What works so far" (decode appends one new token at its
  * absolute position, then paged attention over the sequence's pages).
  */
@@ -302,8 +306,13 @@ int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches)
  *  - num_seqs > PKV_NOALLOC_MAX_SEQS returns PKV_ERR_NOALLOC_LIMIT and enqueues nothing.
  *  - The first call on a device (with that device current) looks up the array's device
  *    address once; make that first call before any stream capture on that device.
- *  - The first call on a device also clears the array once (its merge counters must
- *    start at zero; every completed call leaves them at zero again).
+ *  - The first call on a device also clears the array once, enqueued on that call's
+ *    stream ahead of its kernel (the merge counters must start at zero; every completed
+ *    call leaves them at zero again).  A later call on another stream must be ordered
+ *    after that first call, like any two calls (see below).
+ *  - The looked-up address is kept for the life of the process: after cudaDeviceReset
+ *    (or any re-creation of the device's primary context) this entry point is not
+ *    supported on that device.
  *  - All calls on a device share the one array and it keeps the last call's contents;
  *    calls that overlap on the GPU - on different streams, or from different host
  *    threads without ordering - race on it: serialise them.
@@ -315,7 +324,54 @@ int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *out, const v
                                        const int32_t *context_lens, int num_seqs, int max_context,
                                        float scale, int32_t *device_status, void *stream);
 
-/* ---- host page allocator and continuous-batching scheduler (no GPU) --------------------
+/* ---- host page allocator (no GPU) ------------------------------------------------------
+ *
+ * The admission credits, lazy page assignment and page release that the scheduler below
+ * is built from, for a caller that runs its own scheduler.  The allocator owns the pool's
+ * free list and a host block table [max_seqs][num_layers][max_blocks] (max_blocks =
+ * ceil(max_context / page_tokens), -1 = unassigned) that a caller copies to the device for
+ * the attention calls.  Host memory only; not thread-safe (one caller thread at a time).
+ *
+ * Cited: samir-vllm README, "Current scope" (admission credits = pages for prompt + new - 1
+ * tokens, rounded up to 16-token pages, in every layer; the new-token budget is clamped to
+ * the context limit; credits are separate from physical pages, which are assigned lazily;
+ * a request larger than the whole pool is rejected; completion returns pages and credits);
+ * tiny-vllm part 3, "Distributing K/V into paged blocks" (a page is popped from the back of
+ * the free list when a block is first written; -1 marks an unassigned block).
+ */
+typedef struct pkv_alloc pkv_alloc;
+
+/* free_order: host, nullable - the initial free list (num_pages distinct ids, popped from the
+ * back; pass a seeded permutation for a shuffled pool); NULL means 0 .. num_pages-1.
+ * Returns PKV_OK, PKV_ERR_NULL (out) or PKV_ERR_SHAPE. */
+int pkv_alloc_create(int num_pages, int num_layers, int page_tokens, int max_context, int max_seqs,
+                     const int32_t *free_order, pkv_alloc **out);
+void pkv_alloc_destroy(pkv_alloc *alloc);
+/* Admit a request into sequence seq (0 .. max_seqs-1, not admitted now): reserve its credits,
+ * ceil((prompt + new - 1) / page_tokens) * num_layers with new = min(max_new_tokens,
+ * max_context + 1 - prompt_tokens).  *credits (nullable) receives that count whatever the
+ * outcome.  Returns PKV_OK; PKV_ERR_EXCEEDS_POOL if the credits exceed the whole pool (the
+ * request can never be admitted); PKV_ERR_NO_CREDIT if they do not fit beside the credits
+ * already held (nothing reserved: retry after a sequence is freed); PKV_ERR_STATE if seq is
+ * admitted already; PKV_ERR_SHAPE for prompt < 1, prompt > max_context, max_new_tokens < 1 or
+ * seq out of range. */
+int pkv_alloc_admit(pkv_alloc *alloc, int seq, int prompt_tokens, int max_new_tokens, int32_t *credits);
+/* Physical page of logical block `block` of (seq, layer): the table entry when assigned,
+ * else the page popped from the back of the free list (the first write of that block).
+ * The slot of token t is then page * page_tokens + t % page_tokens with block = t / page_tokens.
+ * Returns PKV_OK, PKV_ERR_NO_PAGE (free list empty; cannot happen while every sequence
+ * stays within its credits), PKV_ERR_STATE (seq not admitted) or PKV_ERR_SHAPE. */
+int pkv_alloc_page(pkv_alloc *alloc, int seq, int layer, int block, int32_t *page);
+/* Return every page of seq to the free list (layers in order, blocks ascending, each pushed on
+ * the back) and release its credits; its table rows become -1.  PKV_OK, PKV_ERR_STATE (seq not
+ * admitted) or PKV_ERR_SHAPE. */
+int pkv_alloc_free_seq(pkv_alloc *alloc, int seq);
+/* The allocator's block table [max_seqs][num_layers][max_blocks] (valid until destroy). */
+const int32_t *pkv_alloc_block_tables(const pkv_alloc *alloc);
+/* Pages on the free list and credits held now (either pointer nullable). */
+int pkv_alloc_state(const pkv_alloc *alloc, int32_t *free_pages, int32_t *credits_in_use);
+
+/* ---- continuous-batching scheduler (no GPU) ----------------------------------------------
  *
  * Cited: samir-vllm README, "What works so far" (requests share the pool; static and
  * continuous batching admit queued prompts by page budget and return pages and budgets on

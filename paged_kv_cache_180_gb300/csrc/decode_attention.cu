@@ -502,24 +502,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     }
     const int valid = min(kPageTokens, w.ctx - w.lp * kPageTokens);
     if (a.slot_mapping != nullptr && w.lp == w.n - 1 && !aborted) {
-      // Fused append: the new token is the last of this page.  Lanes 0-7 move its K row of
-      // head g (16 B each), lanes 8-15 its V row, into the stage (swizzled position) and the pool.
+      // Fused append: the new token is the last of this page, so its slot must be
+      // page * 16 + (ctx - 1) % 16 for this page's block-table entry.  Any other slot is
+      // reported and ignored (the cached row is attended as it is, nothing is stored).
+      // Lanes 0-7 move its K row of head g (16 B each), lanes 8-15 its V row, into the
+      // stage (swizzled position) and the pool.
       const long long slot = __ldg(a.slot_mapping + w.s);
-      if (slot >= 0 && lane < 16) {
-        const int r = valid - 1, c = lane & 7, is_v = lane >> 3;
-        const uint4 x = __ldg((is_v ? a.v_new : a.k_new) + ((long long)w.s * kKvHeads + g) * 8 + c);
-        if (sm.stage_ok[st]) {
-          uint8_t *row = sm.kv[st][is_v] + (g * kPageTokens + r) * kRowBytes;
-          *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = x;
-        }
-        if (slot < a.num_slots) {
-          uint8_t *dst = (is_v ? a.v_pool : a.k_pool) + (slot / kPageTokens) * a.page_stride +
-                         (long long)(g * kPageTokens + slot % kPageTokens) * kRowBytes + c * 16;
+      if (slot >= 0) {
+        const long long page = __ldg(a.block_tables + (long long)w.s * a.bt_stride + w.lp);
+        const int r = valid - 1;
+        const bool ok = slot == page * kPageTokens + r && slot < a.num_slots;
+        if (ok && lane < 16) {
+          const int c = lane & 7, is_v = lane >> 3;
+          const uint4 x = __ldg((is_v ? a.v_new : a.k_new) + ((long long)w.s * kKvHeads + g) * 8 + c);
+          if (sm.stage_ok[st]) {
+            uint8_t *row = sm.kv[st][is_v] + (g * kPageTokens + r) * kRowBytes;
+            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = x;
+          }
+          uint8_t *dst = (is_v ? a.v_pool : a.k_pool) + page * a.page_stride +
+                         (long long)(g * kPageTokens + r) * kRowBytes + c * 16;
           *reinterpret_cast<uint4 *>(dst) = x;
-        } else if (g == 0 && lane == 0) {
+          fence_proxy_async_smem();  // these generic stores precede the stage's next TMA refill
+        } else if (!ok && g == 0 && lane == 0) {
           report(a.status, PKV_DEV_BAD_SLOT);
         }
-        fence_proxy_async_smem();  // these generic stores precede the stage's next TMA refill
       }
       __syncwarp();
     }
@@ -829,9 +835,10 @@ extern "C" int pkv_paged_decode_attention_ctas(const pkv_pool *pool, float *out,
 // a fixed device array of this file, sized for PKV_NOALLOC_MAX_SEQS sequences,
 // for callers that cannot allocate device memory.  On the first call with a
 // device current, its device address is looked up (cudaGetSymbolAddress) and the
-// array is cleared once (the ticket counters must start at zero; every completed
-// call leaves them at zero again).  The call then follows the regular path with
-// that address as the workspace.
+// array is cleared once on the caller's stream, ahead of that call's kernel (the
+// ticket counters must start at zero; every completed call leaves them at zero
+// again).  The call then follows the regular path with that address as the
+// workspace.
 namespace pkv {
 namespace {
 
@@ -845,8 +852,11 @@ static __device__ __align__(256) unsigned char pkv_noalloc_scratch[pkv::kNoalloc
 namespace pkv {
 namespace {
 
-// Device address of pkv_noalloc_scratch on the current device (cleared on first use), or nullptr.
-void *noalloc_scratch_address() {
+// Device address of pkv_noalloc_scratch on the current device, or nullptr.  The first
+// call per device enqueues the clear on `stream`, so the kernel enqueued after it on the
+// same stream sees a zeroed array whatever kind of stream it is (a non-blocking stream
+// is not ordered after work on the legacy default stream).
+void *noalloc_scratch_address(cudaStream_t stream) {
   static std::mutex mu;
   static void *addr[64] = {nullptr};
   int dev = 0;
@@ -861,7 +871,7 @@ void *noalloc_scratch_address() {
       cudaGetLastError();
       return nullptr;
     }
-    if (cudaMemset(p, 0, kNoallocScratchBytes) != cudaSuccess) {
+    if (cudaMemsetAsync(p, 0, kNoallocScratchBytes, stream) != cudaSuccess) {
       cudaGetLastError();
       return nullptr;
     }
@@ -881,7 +891,7 @@ extern "C" int pkv_paged_decode_attention_noalloc(const pkv_pool *pool, float *o
   if (num_seqs <= 0) {
     return num_seqs < 0 ? PKV_ERR_SHAPE : PKV_OK;
   }
-  void *scratch = pkv::noalloc_scratch_address();
+  void *scratch = pkv::noalloc_scratch_address(static_cast<cudaStream_t>(stream));
   if (scratch == nullptr) return PKV_ERR_CUDA;
   return pkv::decode(pool, out, q, num_q_heads, block_tables, block_table_stride, context_lens, num_seqs,
                      max_context, scale, scratch, pkv::kNoallocScratchBytes, device_status, 0, stream);
