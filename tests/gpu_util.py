@@ -90,3 +90,37 @@ class DeviceDecode:
     def status_value(self) -> int:
         torch.cuda.synchronize()
         return int(self.status.item())
+
+
+def oracle_decode_threaded(wl, layer: int = 0, seqs=None):
+    """The oracle's decode attention for every (or the chosen) sequence of ``wl``, one sequence
+    per host thread: each thread draws its sequence's K/V, appends them into one shared oracle
+    pool (sequences own disjoint pages) and attends.  Returns (out [num_seqs, H, D] float64,
+    OR of the error bits).  The C calls release the GIL, so a 256 x 2048 batch takes seconds."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    chosen = range(wl.num_seqs) if seqs is None else seqs
+    pool = oracle.Pool(wl.num_pages, wl.page_tokens, wl.num_kv_heads, wl.head_dim)
+    q = wl.q(layer)
+    bt = np.ascontiguousarray(wl.block_tables[:, layer, :])
+    lens = np.ascontiguousarray(wl.context_lens)
+    out = np.zeros((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=np.float64)
+
+    def one(s):
+        c = int(lens[s])
+        if c > 0 and wl.has_pages(s):
+            k, v = wl.kv_tokens(s, layer)
+            assert oracle.kv_append(pool, k, v, wl.slot_mapping(s, layer, 0, c)) == 0
+        o, err = oracle.paged_decode_attention(pool, q[s:s + 1], bt[s:s + 1], lens[s:s + 1], wl.scale,
+                                               wl.max_context)
+        out[s] = o[0]
+        return err
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        errs = list(ex.map(one, chosen))
+    bits = 0
+    for e in errs:
+        bits |= e
+    return out, bits

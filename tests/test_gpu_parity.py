@@ -198,25 +198,43 @@ def test_workspace_reuse_and_repeat_is_deterministic():
 
 
 # ---------------------------------------------------------------------------
-def test_bandwidth_config_full_size_sampled():
+def test_bandwidth_config_full_size_all_sequences():
     """Batch 256 x context 2048 (1 GiB pool) in the automatic launch configuration the bench times;
-    sampled sequences checked element by element against the oracle."""
+    every sequence checked element by element against the oracle (one host thread per sequence)."""
     wl = configs.bandwidth()
     d = U.DeviceDecode(wl, fill_nan=False, generate_on_device=True)
     d.append_all()
     out = d.attend().cpu().double().numpy()
     assert d.status_value() == 0
-    sample = [0, 1, 77, 128, 200, 255]
-    # the device generator reproduces the host stream bit for bit on the sampled sequences
+    # the device generator reproduces the host stream bit for bit (checked on one sequence)
     from workloads import torch_gen
     kd, vd, _ = torch_gen.workload_kv(wl, 0, U.dev(), seqs=[77])
     kh, vh = wl.kv_tokens(77)
     assert np.array_equal(U.bits(kd), kh) and np.array_equal(U.bits(vd), vh)
-    ref, err, _ = oracle.decode_workload(wl, seqs=sample)
+    ref, err = U.oracle_decode_threaded(wl)
     assert err == 0
-    U.assert_close(out[sample], ref[sample], "bandwidth sample")
-    # every output is a convex combination of V rows: finite and inside [min V, max V] per row
-    assert np.isfinite(out).all()
+    U.assert_close(out, ref, "bandwidth, all 256 sequences")
+
+
+# Equal-length batches in the automatic launch configuration (2 CTAs per SM, 304 on a
+# 152-SM GB300) reach each branch of the kernel's split choice:
+#  * n <= CTAs, each sequence cut into k > 1 equal parts and merged: 8 x 2048 (256 CTAs of
+#    4 pages, 32 parts per sequence, merged in two levels) and 32 x 1024 (288 CTAs, 9 parts);
+#  * n > CTAs with a divisor of n: whole sequences per CTA, 512 x 2048 (256 CTAs of 2
+#    sequences, 2 GiB pool) and 608 x 512 (304 CTAs of 2);
+#  * n > CTAs with no divisor in range (331 is prime): the even page split, every CTA's
+#    range cutting sequences, 331 x 256.
+@pytest.mark.parametrize("num_seqs,context", [(8, 2048), (32, 1024), (512, 2048), (608, 512), (331, 256)],
+                         ids=["cut_8x2048", "cut_32x1024", "whole_512x2048", "whole_608x512", "prime_331x256"])
+def test_equal_length_automatic_split_branches(num_seqs, context):
+    wl = configs.custom(520 + num_seqs, [context] * num_seqs, name=f"equal_{num_seqs}x{context}")
+    d = U.DeviceDecode(wl, fill_nan=True, generate_on_device=True)
+    d.append_all()
+    out = d.attend().cpu().double().numpy()
+    assert d.status_value() == 0
+    ref, err = U.oracle_decode_threaded(wl)
+    assert err == 0
+    U.assert_close(out, ref, wl.name)
 
 
 def test_one_workspace_across_batch_sizes_and_splits():
@@ -284,6 +302,38 @@ def test_decode_step_with_skipped_appends_and_partial_pages():
 
 def test_decode_step_llama_layers():
     _decode_step_case(configs.llama_step(), layers=(0, 7, 15))
+
+
+def test_decode_step_checks_the_new_tokens_slot():
+    """The fused append stores a sequence's new token only at position ctx - 1 of its block
+    table.  Another slot in the pool (an earlier row of the same page, another sequence's
+    decode slot) or a slot past the pool sets PKV_DEV_BAD_SLOT, stores nothing and leaves the
+    cached row in the softmax; a correct slot in the same call is stored and attended."""
+    import paged_kv_cache_180_gb300 as pkv
+    wl = configs.custom(497, [40, 16, 1, 300], name="slot_check")
+    d = U.DeviceDecode(wl)
+    d.append_all()                                    # every token cached, decode tokens included
+    kn, vn, sn = wl.decode_tokens(0)
+    r = np.random.default_rng(7)
+    kn2 = rng.f64_to_bf16_bits(r.standard_normal(kn.shape))
+    vn2 = rng.f64_to_bf16_bits(r.standard_normal(vn.shape))
+    slots = sn.copy()
+    slots[0] = sn[0] - 1                 # the row before the new token, same page
+    slots[1] = sn[3]                     # sequence 3's decode slot
+    slots[2] = wl.num_pages * 16 + 5     # past the pool
+    blocks = wl.max_blocks
+    pkv.decode_step(d.pool, U.to_dev(kn2), U.to_dev(vn2), U.to_dev(slots), d.out, d.q(0), d.bt.view(-1),
+                    wl.num_layers * blocks, d.lens, wl.max_context, wl.scale, d.ws, d.status)
+    assert d.status_value() == 1         # PKV_DEV_BAD_SLOT
+    # expected: the cached pool, with only sequence 3's new token replaced
+    _, err, opool = oracle.decode_workload(wl)
+    assert err == 0
+    assert oracle.kv_append(opool, kn2[3:4], vn2[3:4], sn[3:4]) == 0
+    np.testing.assert_array_equal(U.bits(d.pool.view()).reshape(-1), opool.data.reshape(-1))
+    bt = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    ref, err = oracle.paged_decode_attention(opool, wl.q(0), bt, wl.context_lens, wl.scale, wl.max_context)
+    assert err == 0
+    U.assert_close(d.out.cpu().double().numpy(), ref, "decode_step with checked slots")
 
 
 @pytest.mark.parametrize("overlap", [False, True], ids=["serial", "overlap_previous"])
