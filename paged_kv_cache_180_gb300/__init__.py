@@ -9,7 +9,7 @@ missing that raises ImportError (there is no fallback path).
 """
 _PUBLIC = ("KVPool", "PkvError", "PkvPool", "decode_max_ctas", "decode_plan", "decode_step", "decode_workspace", "decode_workspace_bytes",
            "kv_append", "kv_pool_bytes", "kv_pool_create", "paged_decode_attention",
-           "paged_decode_attention_noalloc", "paged_prefill_attention", "Scheduler",
+           "paged_decode_attention_noalloc", "paged_prefill_attention", "Scheduler", "Allocator",
            "status_string")
 
 

@@ -79,6 +79,13 @@ EXPORTS = {
     "pkv_paged_prefill_attention": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, _P]),
     "pkv_paged_prefill_attention_ex": (_I, [_PP, _P, _P, _I, _I, _P, _P, _L, _P, _I, _I, _I, _F, _P, ctypes.c_uint,
                                             _P]),
+    "pkv_alloc_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
+    "pkv_alloc_destroy": (None, [_P]),
+    "pkv_alloc_admit": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_alloc_page": (_I, [_P, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_alloc_free_seq": (_I, [_P, _I]),
+    "pkv_alloc_block_tables": (ctypes.POINTER(ctypes.c_int32), [_P]),
+    "pkv_alloc_state": (_I, [_P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "pkv_sched_create": (_I, [_I, _I, _I, _I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
     "pkv_sched_submit": (_I, [_P, _L, _I, _I]),
@@ -258,6 +265,64 @@ def paged_decode_attention_noalloc(pool: KVPool | PkvPool, out: torch.Tensor, q:
                                                  _ptr(block_tables), block_table_stride, _ptr(context_lens),
                                                  num_seqs, max_context, scale, _ptr(status), _stream(stream))
     _check("pkv_paged_decode_attention_noalloc", rc)
+
+
+class Allocator:
+    """Host page allocator of ``libpkv.so`` (see ``pkv_alloc_*``): admission credits, lazy pages
+    from a LIFO free list, release of a sequence's pages.  Methods raise PkvError on a negative
+    status, except ``admit``, which returns the status (PKV_OK, NO_CREDIT or EXCEEDS_POOL)."""
+
+    OK, NO_CREDIT, EXCEEDS_POOL = 0, -13, -9
+
+    def __init__(self, num_pages: int, num_layers: int = 1, page_tokens: int = 16, max_context: int = 2048,
+                 max_seqs: int = 32, free_order=None):
+        import numpy as np
+        self._np = np
+        self.num_layers, self.max_seqs = num_layers, max_seqs
+        self.max_blocks = -(-max_context // page_tokens)
+        order = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            order = self._order.ctypes.data
+        h = ctypes.c_void_p()
+        _check("pkv_alloc_create", _lib.pkv_alloc_create(num_pages, num_layers, page_tokens, max_context, max_seqs,
+                                                         order, ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.pkv_alloc_destroy(h)
+            self._h = None
+
+    def admit(self, seq: int, prompt_tokens: int, max_new_tokens: int) -> tuple[int, int]:
+        """(status, credits) of admitting a request into ``seq``."""
+        c = ctypes.c_int32(0)
+        rc = _lib.pkv_alloc_admit(self._h, seq, prompt_tokens, max_new_tokens, ctypes.byref(c))
+        if rc not in (self.OK, self.NO_CREDIT, self.EXCEEDS_POOL):
+            raise PkvError("pkv_alloc_admit", rc)
+        return rc, c.value
+
+    def page(self, seq: int, layer: int, block: int) -> int:
+        p = ctypes.c_int32(-1)
+        _check("pkv_alloc_page", _lib.pkv_alloc_page(self._h, seq, layer, block, ctypes.byref(p)))
+        return p.value
+
+    def free_seq(self, seq: int) -> None:
+        _check("pkv_alloc_free_seq", _lib.pkv_alloc_free_seq(self._h, seq))
+
+    def block_tables(self):
+        """A copy of the block table [max_seqs, num_layers, max_blocks]."""
+        n = self.max_seqs * self.num_layers * self.max_blocks
+        ptr = _lib.pkv_alloc_block_tables(self._h)
+        return self._np.ctypeslib.as_array(ptr, shape=(n,)).copy().reshape(self.max_seqs, self.num_layers,
+                                                                           self.max_blocks)
+
+    def state(self) -> tuple[int, int]:
+        """(free pages, credits in use)."""
+        f, c = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check("pkv_alloc_state", _lib.pkv_alloc_state(self._h, ctypes.byref(f), ctypes.byref(c)))
+        return f.value, c.value
 
 
 class Scheduler:

@@ -70,6 +70,7 @@ extern "C" const char *pkv_status_string(int status) {
     case PKV_ERR_EXCEEDS_POOL: return "request page budget exceeds the whole pool";
     case PKV_ERR_NO_PAGE: return "no free page";
     case PKV_ERR_STATE: return "call out of order";
+    case PKV_ERR_NO_CREDIT: return "request credits do not fit beside the admitted ones now (wait)";
     case PKV_ERR_NOALLOC_LIMIT: return "num_seqs above PKV_NOALLOC_MAX_SEQS (fixed scratch of the allocation-free entry point)";
     default: return "unknown status";
   }

@@ -91,7 +91,7 @@ def test_decode_host_checks_return_before_any_launch(binding):
 
 
 def test_status_strings(binding):
-    for code in range(-11, 1):
+    for code in range(-13, 1):
         assert binding.status_string(code) != "unknown status"
     assert binding.status_string(-99) == "unknown status"
 
