@@ -543,9 +543,12 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
         const bool masked = !(key0 + kPfKeys - 1 <= pos && bad == 0);
         uint64_t valid = ~0ull;
         if (masked) {
+          // keys c <= pos - key0 are causal; each invalid page clears its 16 keys
+          const int lim = pos - key0;
+          valid = lim >= kPfKeys - 1 ? ~0ull : (lim < 0 ? 0ull : (2ull << lim) - 1ull);
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (!(key0 + c <= pos && !((bad >> (c / kPageTokens)) & 1))) valid &= ~(1ull << c);
+          for (int pp = 0; pp < kPfPagesPerBlock; ++pp)
+            if ((bad >> pp) & 1) valid &= ~(0xffffull << (pp * kPageTokens));
         }
         const float mx = signed_max(sv, masked, valid, a.neg != 0);  // in units of sigma * s
         // move the reference max only on a row's first block or when this block's max
