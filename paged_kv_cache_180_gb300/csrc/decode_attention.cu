@@ -73,7 +73,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kCtasPerSm = 2;
 constexpr int kMinPagesPerCta = 4;  // least pages a CTA is given (unless the caller fixes the split)
-constexpr int kMergeGroup = 8;      // a sequence cut into more parts merges them in groups of this many first
+constexpr int kMergeOneLevel = 12;  // a sequence cut into at most this many parts is merged in one pass
+constexpr int kMergeGroup = 8;      // a longer one merges groups of this many consecutive parts first
 constexpr int kHeadRowsBytes = kPageTokens * kRowBytes;  // one head's K (or V) rows of a page: 2 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -249,15 +250,15 @@ __device__ __forceinline__ void issue_page(const DecodeArgs &a, Smem &sm, int st
 // query heads 4g .. 4g+3 with
 //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  out = sum_c acc_c 2^(m_c - M) / L
 // (one pass, rescaling as the running maximum grows) and reset the counter.  A sequence
-// in at most kMergeGroup parts is merged at once.  A longer one is merged in two levels,
-// so that no warp reads more than kMergeGroup parts in a row: the parts of each group of
+// in at most kMergeOneLevel parts is merged at once.  A longer one is merged in two levels,
+// so that its first merges overlap its other parts' streaming: the parts of each group of
 // kMergeGroup consecutive CTAs are merged into the group's first slot, and the warp that
 // finishes the last group merges the group results.  The two halves of a ticket may be
 // apart: a warp can take the ticket, stream more pages, and only then look at it.
 
 // First-level merge group [lo, hi] of part c of a sequence cut across c_first .. c_last.
 __device__ __forceinline__ void merge_group(int c, int c_first, int c_last, int &lo, int &hi) {
-  if (c_last - c_first < kMergeGroup) {
+  if (c_last - c_first < kMergeOneLevel) {
     lo = c_first;
     hi = c_last;
     return;
@@ -323,7 +324,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long l
   const int h = g * kGroup + (lane >> 3), d0 = (lane & 7) * 8;
   float M, L, r[8];
   merge_parts(a, s, lo, hi - lo + 1, 1, h, d0, M, L, r);
-  if (c_last - c_first >= kMergeGroup) {
+  if (c_last - c_first >= kMergeOneLevel) {
     // first level done: the group's merged state replaces its first part, then the
     // second-level ticket (lane 0's release covers every lane's stores after __syncwarp)
     Slot &dst = a.slots[(long long)lo + s];
