@@ -329,13 +329,6 @@ def cpu_baseline(wl, reps: int = 3):
                                         f"whole step"}}
 
 
-def cpu_oracle_run(wl, threads: int, reps: int = 3):
-    """Times the FP64 oracle (as it stands) on the whole step of ``wl``; (median seconds, units)."""
-    prep = OracleDecodeStep(wl, threads)
-    times = [prep.run(threads) for _ in range(reps)]
-    return statistics.median(times), len(prep.units)
-
-
 def cpu_baseline_trace(tr, host_steps, step_bytes_list, sample_steps: int = 200, one_thread_steps: int = 50):
     """The oracle replaying the first ``sample_steps`` steps of the continuous-batching trace: each
     step appends its tokens into the oracle's pool and attends over every live slot (threaded over
