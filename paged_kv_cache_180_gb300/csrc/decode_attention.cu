@@ -33,10 +33,13 @@
 //    pages (context 0 or invalid) get zero rows from CTA s % G.
 //  * Staging: each page arrives as two tiled TMA boxes (its K half and its V
 //    half: 8 heads x 16 tokens x 128 B rows, 16 KiB each, contiguous in the
-//    pool) into a ring of kStages shared-memory stages, each with an mbarrier.
-//    There is no producer warp: the CTA has one warp per K/V head, and the last
-//    warp to finish with a stage (a per-stage counter in shared memory; nobody
-//    waits) refills it with the page kStages ahead.  The boxes land 128-byte
+//    pool) into a ring of shared-memory stages, each with an mbarrier: three
+//    stages when two CTAs share an SM, six when the grid has at most one CTA per
+//    SM (the same bytes in flight per SM, and a CTA of a small batch has all of
+//    its pages requested at once).  There is no producer warp: the CTA has one
+//    warp per K/V head, and the last warp to finish with a stage (a per-stage
+//    counter in shared memory; nobody waits) refills it with the page a ring
+//    length ahead.  The boxes land 128-byte
 //    swizzled (16-byte chunk c of row r stored at chunk c ^ (r % 8)), so the
 //    ldmatrix reads below are free of bank conflicts.
 //  * Math on the tensor cores, one warp per K/V head serving its 4 query heads:
@@ -67,7 +70,8 @@
 namespace pkv {
 namespace {
 
-constexpr int kStages = 3;                // pages in flight per warp
+constexpr int kStagesShared = 3;  // ring stages when two CTAs share an SM
+constexpr int kStagesAlone = 6;   // ring stages when the grid has at most one CTA per SM
 constexpr int kWarps = kKvHeads;          // one warp per K/V head
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
@@ -75,6 +79,7 @@ constexpr int kCtasPerSm = 2;
 constexpr int kMinPagesPerCta = 4;  // least pages a CTA is given (unless the caller fixes the split)
 constexpr int kMergeOneLevel = 12;  // a sequence cut into at most this many parts is merged in one pass
 constexpr int kMergeGroup = 8;      // a longer one merges groups of this many consecutive parts first
+constexpr int kMergeBatch = 4;      // partial states read at once by a merging warp
 constexpr int kHeadRowsBytes = kPageTokens * kRowBytes;  // one head's K (or V) rows of a page: 2 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -114,7 +119,8 @@ struct DecodeArgs {
   long long num_slots;  // num_pages * 16
 };
 
-struct __align__(1024) Smem {
+template <int kStages>
+struct __align__(1024) SmemT {
   uint8_t kv[kStages][2][kHalfPageBytes];  // [stage][K|V] boxes of [head][token][128 B], 1024-byte aligned
   uint64_t full[kStages];
   int stage_ok[kStages];
@@ -129,13 +135,15 @@ struct __align__(1024) Smem {
   int seq0;
   int found;
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + slack to align the dynamic base to 1024 B
+template <int kStages>
+constexpr size_t smem_bytes() { return sizeof(SmemT<kStages>) + 1024; }  // + slack to align the base to 1024 B
 
 __device__ __forceinline__ int seq_pages(int ctx, int max_context) {
   return (ctx > 0 && ctx <= max_context) ? (ctx + kPageTokens - 1) / kPageTokens : 0;
 }
 
 // Inclusive block-wide prefix sum (all kThreads threads must call).
+template <class Smem>
 __device__ long long block_inclusive_scan(long long v, Smem &sm, long long *block_total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long long x = v;
@@ -227,6 +235,7 @@ __device__ int effective_ctas(int G, long long T, int n, int pmin, int pmax, int
 
 // Start the copy of the page the walk points at into stage st (or mark the stage
 // empty when the page id is invalid).  One thread calls this.
+template <class Smem>
 __device__ __forceinline__ void issue_page(const DecodeArgs &a, Smem &sm, int st, const Walk &w, uint64_t policy) {
   const int page = __ldg(a.block_tables + (long long)w.s * a.bt_stride + w.lp);
   if (page >= 0 && page < a.num_pages) {
@@ -281,27 +290,45 @@ __device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long g
 
 // Merge of the partial states in slots first + k * stride + s, k < count, for this lane's
 // query head h and dims d0 .. d0 + 7: the running maximum M, sum L and accumulator r.
+// The parts are read kMergeBatch at a time, every load of a batch issued before the first
+// is used, so a batch costs one L2 round trip; the batch's maximum rescales the running
+// state once.
 __device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int first, int count, int stride, int h,
                                             int d0, float &M, float &L, float (&r)[8]) {
   M = -INFINITY;
   L = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) r[i] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < count; ++k) {
-    const Slot &part = a.slots[(long long)first + (long long)k * stride + s];
-    const float2 ml = __ldcg(&part.ml[h]);
-    const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
-    const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
-    // a part whose pages were all invalid has m = -inf and weight 0
-    const float m_new = fmaxf(M, ml.x);
+  for (int k0 = 0; k0 < count; k0 += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float4 x0[kMergeBatch], x1[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (k0 + j < count) {
+        const Slot &part = a.slots[(long long)first + (long long)(k0 + j) * stride + s];
+        ml[j] = __ldcg(&part.ml[h]);
+        x0[j] = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
+        x1[j] = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+      } else {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // a part whose pages were all invalid (or a padding entry) has m = -inf and weight 0
+    float m_new = M;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) m_new = fmaxf(m_new, ml[j].x);
     const float keep = (m_new == -INFINITY) ? 1.f : exp2f(M - m_new);
-    const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - m_new);
-    L = L * keep + ml.y * wgt;
-    r[0] = r[0] * keep + wgt * x0.x; r[1] = r[1] * keep + wgt * x0.y;
-    r[2] = r[2] * keep + wgt * x0.z; r[3] = r[3] * keep + wgt * x0.w;
-    r[4] = r[4] * keep + wgt * x1.x; r[5] = r[5] * keep + wgt * x1.y;
-    r[6] = r[6] * keep + wgt * x1.z; r[7] = r[7] * keep + wgt * x1.w;
+    L *= keep;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] *= keep;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const float wgt = (ml[j].x == -INFINITY) ? 0.f : exp2f(ml[j].x - m_new);
+      L += ml[j].y * wgt;
+      r[0] += wgt * x0[j].x; r[1] += wgt * x0[j].y; r[2] += wgt * x0[j].z; r[3] += wgt * x0[j].w;
+      r[4] += wgt * x1[j].x; r[5] += wgt * x1[j].y; r[6] += wgt * x1[j].z; r[7] += wgt * x1[j].w;
+    }
     M = m_new;
   }
 }
@@ -349,7 +376,9 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long l
   out[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
 }
 
+template <int kStages>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
+  using Smem = SmemT<kStages>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -492,8 +521,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   bool has_first = (w.lp == 0);
   long long gfirst = pa - w.lp;  // global index of the first page of the current sequence
   bool aborted = false;          // a wait gave up: stop waiting, computing and issuing, keep walking
-  int pend_s = -1, pend_n = 0, pend_ticket = 0;  // a cut sequence whose merge check waits for the end
-  long long pend_gfirst = 0;
+  struct Pending {
+    int s, n, ticket;
+    long long gfirst;
+  } pend0 = {-1, 0, 0, 0}, pend1 = {-1, 0, 0, 0};  // cut segments whose merge check waits for the end
 
   for (long long i = 0; i < count; ++i) {
     const int st = int(i % kStages);
@@ -637,17 +668,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
             *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
           if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
         }
+        // The ticket is looked at after the loop, so that its round trip (and a merge) do not
+        // stall the pages that follow.  A range holds at most two cut segments: its first
+        // (begun in an earlier range) and its last (going on in a later one).
         const int ticket = ticket_of(a, w.s, gfirst, w.n, g, lane, T, Gu, cta);
-        if (has_first || i == count - 1) {
-          merge_if_last(a, w.s, gfirst, w.n, g, lane, T, Gu, ticket, cta);
-        } else {
-          // The range began inside this sequence: look at the ticket after the loop,
-          // so its round trip (and a merge) do not stall the pages that follow.
-          pend_s = w.s;
-          pend_gfirst = gfirst;
-          pend_n = w.n;
-          pend_ticket = ticket;
-        }
+        Pending &p = pend0.s < 0 ? pend0 : pend1;
+        p.s = w.s;
+        p.gfirst = gfirst;
+        p.n = w.n;
+        p.ticket = ticket;
       }
       if (i + 1 < count) {
         w.next(a);
@@ -663,7 +692,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       w.next(a);
     }
   }
-  if (pend_s >= 0) merge_if_last(a, pend_s, pend_gfirst, pend_n, g, lane, T, Gu, pend_ticket, cta);
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k) {
+    const Pending p = k == 0 ? pend0 : pend1;
+    if (p.s >= 0) merge_if_last(a, p.s, p.gfirst, p.n, g, lane, T, Gu, p.ticket, cta);
+  }
   named_barrier_sync(1, kThreads);
   if (tid == 0 && sm.any_aborted) {
     // Copies issued for pages nobody consumed: wait (bounded) so none lands after exit.
@@ -693,8 +726,11 @@ int setup_kernel_attributes() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(paged_decode_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kSmemBytes));
+    err = cudaFuncSetAttribute(paged_decode_partial_kernel<kStagesShared>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem_bytes<kStagesShared>()));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(paged_decode_partial_kernel<kStagesAlone>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<kStagesAlone>()));
   });
   return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -746,26 +782,31 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.num_slots = (long long)pool->num_pages * pool->page_tokens;
   const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // A grid with at most one CTA per SM gets the deeper ring: the same bytes in flight per SM
+  // as two CTAs with the shallow one.
+  const bool alone = G <= device_sm_count();
+  void (*kernel)(DecodeArgs) = alone ? paged_decode_partial_kernel<kStagesAlone> : paged_decode_partial_kernel<kStagesShared>;
+  const size_t smem = alone ? smem_bytes<kStagesAlone>() : smem_bytes<kStagesShared>();
   if (flags & PKV_OVERLAP_PREVIOUS) {
     // programmatic stream serialization: the kernel may start while the previous kernel on
     // the stream finishes (see griddep_launch_dependents / griddep_wait in the kernel)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(G));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, paged_decode_partial_kernel, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, a) != cudaSuccess) {
       cudaGetLastError();
       return PKV_ERR_LAUNCH;
     }
     return PKV_OK;
   }
-  paged_decode_partial_kernel<<<G, kThreads, kSmemBytes, st>>>(a);
+  kernel<<<G, kThreads, smem, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
   return PKV_OK;
 }
