@@ -31,6 +31,14 @@
 //    are reset by the merging warps, so a zeroed workspace stays valid across
 //    calls of any batch size.  Sequences with no
 //    pages (context 0 or invalid) get zero rows from CTA s % G.
+//  * Small grids (no more CTAs than can be resident in clusters of 8 at one CTA
+//    per SM) are launched in thread-block clusters of 8 consecutive CTAs, and
+//    the first merge level stays on chip: the CTAs of a cluster that hold parts
+//    of a cut sequence push each head group's partial state into the shared
+//    memory of the cluster CTA that merges that head group (distributed shared
+//    memory stores), one cluster barrier makes them visible, and the merge reads
+//    local shared memory.  Only a sequence cut across clusters still meets in the
+//    workspace, one state per cluster, behind the same atomic tickets.
 //  * Staging: each page arrives as two tiled TMA boxes (its K half and its V
 //    half: 8 heads x 16 tokens x 128 B rows, 16 KiB each, contiguous in the
 //    pool) into a ring of shared-memory stages, each with an mbarrier: three
@@ -72,6 +80,7 @@ namespace {
 
 constexpr int kStagesShared = 3;  // ring stages when two CTAs share an SM
 constexpr int kStagesAlone = 6;   // ring stages when the grid has at most one CTA per SM
+constexpr int kClusterCtas = 8;   // CTAs per cluster when the small-grid kernel merges on chip
 constexpr int kWarps = kKvHeads;          // one warp per K/V head
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtas = 1024;
@@ -92,6 +101,20 @@ struct Slot {
   int counter2[kWarps];          // per head group: merge groups of the sequence done (long sequences); 0 between calls
 };
 
+// Cluster merges: one head group's partial state of one part of a sequence, as the CTA that
+// holds the part pushes it into the shared memory of the CTA that merges that head group.
+struct GroupState {
+  float acc[kGroup][kHeadDim];  // un-normalised sum of p * V of query heads 4g .. 4g+3
+  float2 ml[kGroup];            // (running max in log2 units, sum of p)
+};
+// A sequence held by p <= kClusterCtas CTAs of a cluster has its head group g merged by its
+// CTA g % p, which so receives p parts of at most ceil(kWarps / p) head groups: at most 14
+// (p = 7) states.
+constexpr int kRecvSlots = 14;
+struct RecvArea {
+  GroupState slot[kRecvSlots];  // slot k * ceil(kWarps / p) + g / p: part k, head group g
+};
+
 struct DecodeArgs {
   CUtensorMap tmap_k;  // K halves: dims (64 elems, 128 rows = head*16 + token, pages), 128B swizzle
   CUtensorMap tmap_v;  // V halves, same shape
@@ -106,7 +129,7 @@ struct DecodeArgs {
   float scale_log2;  // scale * log2(e)
   Slot *slots;       // [kMaxCtas + num_seqs] partial states and ticket counters
   int32_t *status;
-  int exact_ctas;    // 1: split over exactly min(gridDim.x, T) CTAs (the caller chose the count)
+  int split_ctas;    // > 0: split over exactly min(split_ctas, T) CTAs (the caller chose the count)
   // Fused append (pkv_decode_step), else null: sequence s's new token (position ctx-1)
   // goes to slot_mapping[s]; its rows replace the stale ones of the last page in shared
   // memory and are written to the pool by the CTA that holds that page.
@@ -135,8 +158,10 @@ struct __align__(1024) SmemT {
   int seq0;
   int found;
 };
-template <int kStages>
-constexpr size_t smem_bytes() { return sizeof(SmemT<kStages>) + 1024; }  // + slack to align the base to 1024 B
+// Dynamic shared memory of a kernel instance: the ring and bookkeeping, then (cluster merges)
+// two receive areas, plus slack to align the base to 1024 B.
+template <int kStages, bool kCluster>
+constexpr size_t smem_bytes() { return sizeof(SmemT<kStages>) + (kCluster ? 2 * sizeof(RecvArea) : 0) + 1024; }
 
 __device__ __forceinline__ int seq_pages(int ctx, int max_context) {
   return (ctx > 0 && ctx <= max_context) ? (ctx + kPageTokens - 1) / kPageTokens : 0;
@@ -203,17 +228,18 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int s, int g, int la
 
 // How many of the G launched CTAs share the T pages of n sequences (pmin .. pmax
 // pages each).  Every choice is at most min(G, T), so no CTA is left without a page.
-//  * exact: the caller fixed the count.
+//  * no pages at all: 0 (every CTA only zeroes the rows of empty sequences).
+//  * split > 0: the caller fixed the count.
 //  * equal-length batches: split along sequence boundaries, so that no CTA holds
 //    the end of one sequence and the start of the next: k CTAs per sequence
 //    when n <= G (k >= 1, at least kMinPagesPerCta pages each), else the largest
 //    divisor of n not above G (whole sequences per CTA) when that keeps at least
 //    half of the CTAs busy.
 //  * otherwise an even split with at least kMinPagesPerCta pages per CTA.
-__device__ int effective_ctas(int G, long long T, int n, int pmin, int pmax, int exact) {
-  if (T <= 0) return 1;
+__device__ int effective_ctas(int G, long long T, int n, int pmin, int pmax, int split) {
+  if (T <= 0) return 0;
+  if (split > 0) return int(T < split ? T : split);
   const long long cap = T < G ? T : G;
-  if (exact) return int(cap);
   if (n > 0 && pmin == pmax) {
     if (n <= G) {
       int k = G / n;
@@ -288,13 +314,13 @@ __device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long g
   return ticket;  // meaningful in lane 0
 }
 
-// Merge of the partial states in slots first + k * stride + s, k < count, for this lane's
-// query head h and dims d0 .. d0 + 7: the running maximum M, sum L and accumulator r.
-// The parts are read kMergeBatch at a time, every load of a batch issued before the first
-// is used, so a batch costs one L2 round trip; the batch's maximum rescales the running
-// state once.
-__device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int first, int count, int stride, int h,
-                                            int d0, float &M, float &L, float (&r)[8]) {
+// Merge of `count` partial states for this lane's query head h and dims d0 .. d0 + 7:
+// the running maximum M, sum L and accumulator r.  read(k, ml, x0, x1) loads part k's
+// (m, l) and accumulator dims d0 .. d0 + 7.  The parts are read kMergeBatch at a time,
+// every load of a batch issued before the first is used, so a batch costs one round
+// trip; the batch's maximum rescales the running state once.
+template <class Read>
+__device__ __forceinline__ void merge_states(int count, Read read, float &M, float &L, float (&r)[8]) {
   M = -INFINITY;
   L = 0.f;
 #pragma unroll
@@ -305,10 +331,7 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int firs
 #pragma unroll
     for (int j = 0; j < kMergeBatch; ++j) {
       if (k0 + j < count) {
-        const Slot &part = a.slots[(long long)first + (long long)(k0 + j) * stride + s];
-        ml[j] = __ldcg(&part.ml[h]);
-        x0[j] = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
-        x1[j] = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+        read(k0 + j, ml[j], x0[j], x1[j]);
       } else {
         ml[j] = make_float2(-INFINITY, 0.f);
         x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -331,6 +354,28 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int firs
     }
     M = m_new;
   }
+}
+
+// merge_states over the workspace slots first + k * stride + s, k < count (L2 reads).
+__device__ __forceinline__ void merge_parts(const DecodeArgs &a, int s, int first, int count, int stride, int h,
+                                            int d0, float &M, float &L, float (&r)[8]) {
+  merge_states(
+      count,
+      [&](int k, float2 &ml, float4 &x0, float4 &x1) {
+        const Slot &part = a.slots[(long long)first + (long long)k * stride + s];
+        ml = __ldcg(&part.ml[h]);
+        x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
+        x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+      },
+      M, L, r);
+}
+
+// Writes the merged rows of query head h, dims d0 .. d0 + 7 of sequence s.
+__device__ __forceinline__ void write_merged(const DecodeArgs &a, int s, int h, int d0, float L, const float (&r)[8]) {
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float4 *out = reinterpret_cast<float4 *>(a.out + ((long long)s * kQHeads + h) * kHeadDim + d0);
+  out[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
+  out[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
 }
 
 __device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long long gfirst, int n, int g, int lane,
@@ -370,23 +415,105 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs &a, int s, long l
     __syncwarp();
     merge_parts(a, s, c_first, groups, kMergeGroup, h, d0, M, L, r);
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  float4 *out = reinterpret_cast<float4 *>(a.out + ((long long)s * kQHeads + h) * kHeadDim + d0);
-  out[0] = make_float4(r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv);
-  out[1] = make_float4(r[4] * inv, r[5] * inv, r[6] * inv, r[7] * inv);
+  write_merged(a, s, h, d0, L, r);
 }
 
-template <int kStages>
+// Cluster merges (launches with clusters of kClusterCtas consecutive CTAs; CTA c has cluster
+// rank c % kClusterCtas).  Sequence s (pages gfirst .. gfirst + n - 1, cut across CTAs
+// c_first .. c_last) has parts in CTAs lo .. hi of a cluster, p = hi - lo + 1 of them.  Head
+// group g of these parts is merged by warp g of CTA lo + g % p: the CTA holding part k
+// pushes it into that CTA's receive area (area 1 when s reaches the end of the receiving
+// CTA's range, else area 0: a CTA receives for at most its first and its last segment),
+// slot k * ceil(kWarps / p) + g / p.
+struct ClusterPlan {
+  int c_first, c_last, cl0, lo, p;
+  int recv;  // CTA that merges this warp's head group
+  int slot;  // its receive slot for part 0 (part k: + k * qmax)
+  int qmax;
+  int area;  // receive area of s in CTA recv
+};
+
+__device__ __forceinline__ ClusterPlan cluster_plan(long long gfirst, int n, int g, long long T, int Gu, int cta) {
+  ClusterPlan c;
+  c.c_first = cta_of_page(gfirst, T, Gu);
+  c.c_last = cta_of_page(gfirst + n - 1, T, Gu);
+  c.cl0 = cta - cta % kClusterCtas;
+  c.lo = max(c.c_first, c.cl0);
+  c.p = min(c.c_last, c.cl0 + kClusterCtas - 1) - c.lo + 1;
+  c.recv = c.lo + g % c.p;
+  c.qmax = (kWarps + c.p - 1) / c.p;
+  c.slot = g / c.p;
+  c.area = gfirst + n - 1 >= (long long)(c.recv + 1) * T / Gu - 1 ? 1 : 0;
+  return c;
+}
+
+// After the cluster barrier that follows every push: if this CTA merges head group g of s,
+// warp g merges the p parts from its receive area.  When s lies in this cluster alone the
+// rows are written out; otherwise the cluster's state goes to workspace slot lo + s, and the
+// warp that takes the last ticket on a counter of slot c_first + s merges the clusters'
+// states from the workspace, as the two-level merge does.
+__device__ __forceinline__ void cluster_merge(const DecodeArgs &a, const RecvArea *recv, int s, long long gfirst,
+                                              int n, int g, int lane, long long T, int Gu, int cta) {
+  const ClusterPlan c = cluster_plan(gfirst, n, g, T, Gu, cta);
+  if (cta != c.recv) return;  // another CTA of this cluster merges this head group
+  const int hl = lane >> 3, h = g * kGroup + hl, d0 = (lane & 7) * 8;
+  float M, L, r[8];
+  merge_states(
+      c.p,
+      [&](int k, float2 &ml, float4 &x0, float4 &x1) {
+        const GroupState &gs = recv[c.area].slot[k * c.qmax + c.slot];
+        ml = gs.ml[hl];
+        x0 = *reinterpret_cast<const float4 *>(&gs.acc[hl][d0]);
+        x1 = *reinterpret_cast<const float4 *>(&gs.acc[hl][d0 + 4]);
+      },
+      M, L, r);
+  if (c.c_first >= c.cl0 && c.c_last < c.cl0 + kClusterCtas) {
+    write_merged(a, s, h, d0, L, r);
+    return;
+  }
+  // this cluster's state, then the ticket (lane 0's release covers every lane's stores after __syncwarp)
+  Slot &dst = a.slots[(long long)c.lo + s];
+  __stcg(reinterpret_cast<float4 *>(&dst.acc[h][d0]), make_float4(r[0], r[1], r[2], r[3]));
+  __stcg(reinterpret_cast<float4 *>(&dst.acc[h][d0 + 4]), make_float4(r[4], r[5], r[6], r[7]));
+  if ((lane & 7) == 0) __stcg(&dst.ml[h], make_float2(M, L));
+  __syncwarp();
+  const int k0 = c.c_first / kClusterCtas, k1 = c.c_last / kClusterCtas;
+  int last = 0;
+  if (lane == 0) {
+    last = atomic_add_acq_rel_gpu(&a.slots[(long long)c.c_first + s].counter[g], 1) == k1 - k0;
+    if (last) atomicExch(&a.slots[(long long)c.c_first + s].counter[g], 0);  // ready for the next call
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __syncwarp();  // lane 0's acquire comes before every lane's reads of the clusters' states
+  merge_states(
+      k1 - k0 + 1,
+      [&](int k, float2 &ml, float4 &x0, float4 &x1) {
+        const Slot &part = a.slots[(long long)(k == 0 ? c.c_first : (k0 + k) * kClusterCtas) + s];
+        ml = __ldcg(&part.ml[h]);
+        x0 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0]));
+        x1 = __ldcg(reinterpret_cast<const float4 *>(&part.acc[h][d0 + 4]));
+      },
+      M, L, r);
+  write_merged(a, s, h, d0, L, r);
+}
+
+template <int kStages, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
   using Smem = SmemT<kStages>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
+  // cluster merges: the partial states other CTAs of the cluster push to this one
+  RecvArea *recv = reinterpret_cast<RecvArea *>(reinterpret_cast<uint8_t *>(&sm) + sizeof(Smem));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   // Launched with overlap (PKV_OVERLAP_PREVIOUS), the next kernel may start its own set-up
   // now; this one reads the lengths, tables and pool pages at once, and q, the new rows and
   // every global write wait (griddep_wait) until the kernel before it has completed.
   griddep_launch_dependents();
+  // cluster merges: no CTA writes into another's shared memory before every CTA of the cluster
+  // has started (this arrival, and the wait before the page loop)
+  if constexpr (kCluster) cluster_arrive_relaxed();
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -394,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       sm.stage_done[i] = 0;
     }
     sm.found = 0;
+    sm.seq0 = 0;
+    sm.seq0_first = 0;
     sm.issued = 0;
     sm.any_aborted = 0;
     mbar_init_fence();
@@ -439,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       hi = max(hi, sm.warp_pmax[w]);
     }
     sm.total_pages = t;
-    sm.used_ctas = effective_ctas(G, t, n, lo, hi, a.exact_ctas);
+    sm.used_ctas = effective_ctas(G, t, n, lo, hi, a.split_ctas);
   }
   __syncthreads();
   const long long T = sm.total_pages;
@@ -458,6 +587,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     griddep_wait();
     if (bad_context) report(a.status, PKV_DEV_BAD_CONTEXT);
     zero_empty_rows();
+    if constexpr (kCluster) {
+      // the cluster barriers of the CTAs that hold pages: the start, and after every push
+      cluster_wait();
+      cluster_sync();
+    }
     return;
   }
   const long long pa = (long long)cta * T / Gu, pb = (long long)(cta + 1) * T / Gu;
@@ -503,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
   griddep_wait();
   if (bad_context) report(a.status, PKV_DEV_BAD_CONTEXT);
   zero_empty_rows();
+  if constexpr (kCluster) cluster_wait();  // every CTA of the cluster has started
 
   const int quad = lane & 3;     // column pair of the accumulator fragments
   const int hrow = lane >> 2;    // fragment row: query head hrow of the group when < 4
@@ -660,18 +795,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
                 make_float2((o[nd][0] + o[nd][2]) * inv, (o[nd][1] + o[nd][3]) * inv);
         }
       } else {
-        Slot &mine = a.slots[(long long)cta + w.s];
+        // the partial state: into the workspace slot cta + s, or (cluster merges) pushed into
+        // the receive area of the CTA that merges this head group
         if (hrow < kGroup) {
-          float *dst = &mine.acc[g * kGroup + hrow][2 * quad];
+          if constexpr (kCluster) {
+            const ClusterPlan c = cluster_plan(gfirst, w.n, g, T, Gu, cta);
+            GroupState &dst = recv[c.area].slot[(cta - c.lo) * c.qmax + c.slot];  // its address in CTA c.recv
+            const uint32_t rank = uint32_t(c.recv - c.cl0);
+            const uint32_t acc = cluster_map(smem_addr(&dst.acc[hrow][2 * quad]), rank);
 #pragma unroll
-          for (int nd = 0; nd < 8; ++nd)
-            *reinterpret_cast<float2 *>(dst + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
-          if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
+            for (int nd = 0; nd < 8; ++nd)
+              st_cluster_f2(acc + 32u * nd, make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]));
+            if (quad == 0) st_cluster_f2(cluster_map(smem_addr(&dst.ml[hrow]), rank), make_float2(m_run, lt));
+          } else {
+            Slot &mine = a.slots[(long long)cta + w.s];
+            float *acc = &mine.acc[g * kGroup + hrow][2 * quad];
+#pragma unroll
+            for (int nd = 0; nd < 8; ++nd)
+              *reinterpret_cast<float2 *>(acc + 8 * nd) = make_float2(o[nd][0] + o[nd][2], o[nd][1] + o[nd][3]);
+            if (quad == 0) mine.ml[g * kGroup + hrow] = make_float2(m_run, lt);
+          }
         }
         // The ticket is looked at after the loop, so that its round trip (and a merge) do not
         // stall the pages that follow.  A range holds at most two cut segments: its first
         // (begun in an earlier range) and its last (going on in a later one).
-        const int ticket = ticket_of(a, w.s, gfirst, w.n, g, lane, T, Gu, cta);
+        int ticket = 0;
+        if constexpr (!kCluster) ticket = ticket_of(a, w.s, gfirst, w.n, g, lane, T, Gu, cta);
         Pending &p = pend0.s < 0 ? pend0 : pend1;
         p.s = w.s;
         p.gfirst = gfirst;
@@ -692,10 +841,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       w.next(a);
     }
   }
+  if constexpr (kCluster) {
+    cluster_sync();  // every push of the cluster has landed
 #pragma unroll 1
-  for (int k = 0; k < 2; ++k) {
-    const Pending p = k == 0 ? pend0 : pend1;
-    if (p.s >= 0) merge_if_last(a, p.s, p.gfirst, p.n, g, lane, T, Gu, p.ticket, cta);
+    for (int k = 0; k < 2; ++k) {
+      const Pending p = k == 0 ? pend0 : pend1;
+      if (p.s >= 0) cluster_merge(a, recv, p.s, p.gfirst, p.n, g, lane, T, Gu, cta);
+    }
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+      const Pending p = k == 0 ? pend0 : pend1;
+      if (p.s >= 0) merge_if_last(a, p.s, p.gfirst, p.n, g, lane, T, Gu, p.ticket, cta);
+    }
   }
   named_barrier_sync(1, kThreads);
   if (tid == 0 && sm.any_aborted) {
@@ -722,17 +880,85 @@ int auto_ctas(int num_seqs, int max_context) {
   return int(g);
 }
 
+// The three kernel instances: two CTAs per SM with the shallow ring; one CTA per SM with the
+// deep ring; the same in clusters of kClusterCtas that merge cut sequences on chip.
+using KernelFn = void (*)(DecodeArgs);
+constexpr KernelFn kKernelShared = paged_decode_partial_kernel<kStagesShared, false>;
+constexpr KernelFn kKernelAlone = paged_decode_partial_kernel<kStagesAlone, false>;
+constexpr KernelFn kKernelCluster = paged_decode_partial_kernel<kStagesAlone, true>;
+
 int setup_kernel_attributes() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(paged_decode_partial_kernel<kStagesShared>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(smem_bytes<kStagesShared>()));
+    err = cudaFuncSetAttribute(kKernelShared, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem_bytes<kStagesShared, false>()));
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(paged_decode_partial_kernel<kStagesAlone>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<kStagesAlone>()));
+      err = cudaFuncSetAttribute(kKernelAlone, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes<kStagesAlone, false>()));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(kKernelCluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes<kStagesAlone, true>()));
   });
   return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Most CTAs of the clustered instance resident at once on the current device (a multiple of
+// kClusterCtas), 0 when it cannot be determined.
+int cluster_capacity() {
+  static std::mutex mu;
+  static int cap[64];
+  static bool known[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    if (setup_kernel_attributes() != PKV_OK) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<kStagesAlone, true>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kKernelCluster, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cap[dev] = n > 0 ? n * kClusterCtas : 0;
+    known[dev] = true;
+  }
+  return cap[dev];
+}
+
+// Kernel instance and grid for a split over G CTAs: clusters when there is more than one CTA
+// and every cluster of the grid can be resident at once (a grid the kernel sizes itself that
+// would fit the SMs but not the clusters is cut to the cluster capacity), else one CTA per SM
+// with the deep ring when G fits the SMs, else two CTAs per SM.
+struct LaunchChoice {
+  KernelFn kernel;
+  size_t smem;
+  int grid;
+  int cluster;  // CTAs per cluster, 1 without
+};
+
+LaunchChoice choose_launch(int G, bool caller_chose) {
+  const int cap = cluster_capacity();
+  if (!caller_chose && G > cap && G <= device_sm_count()) G = cap;
+  if (G >= 2 && G <= cap) {
+    const int grid = (G + kClusterCtas - 1) / kClusterCtas * kClusterCtas;
+    return {kKernelCluster, smem_bytes<kStagesAlone, true>(), grid, kClusterCtas};
+  }
+  if (G <= device_sm_count()) return {kKernelAlone, smem_bytes<kStagesAlone, false>(), G, 1};
+  return {kKernelShared, smem_bytes<kStagesShared, false>(), G, 1};
 }
 
 int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, const int32_t *block_tables,
@@ -772,7 +998,7 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.slots = static_cast<Slot *>(workspace);
   a.status = device_status;
 
-  a.exact_ctas = num_ctas > 0 ? 1 : 0;
+  a.split_ctas = num_ctas;
   a.k_new = static_cast<const uint4 *>(k_new);
   a.v_new = static_cast<const uint4 *>(v_new);
   a.slot_mapping = slot_mapping;
@@ -780,34 +1006,34 @@ int decode(const pkv_pool *pool, float *out, const void *q, int num_q_heads, con
   a.v_pool = static_cast<uint8_t *>(pool->v_base);
   a.page_stride = pool->page_stride_bytes;
   a.num_slots = (long long)pool->num_pages * pool->page_tokens;
-  const int G = num_ctas > 0 ? num_ctas : auto_ctas(num_seqs, max_context);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // A grid with at most one CTA per SM gets the deeper ring: the same bytes in flight per SM
-  // as two CTAs with the shallow one.
-  const bool alone = G <= device_sm_count();
-  void (*kernel)(DecodeArgs) = alone ? paged_decode_partial_kernel<kStagesAlone> : paged_decode_partial_kernel<kStagesShared>;
-  const size_t smem = alone ? smem_bytes<kStagesAlone>() : smem_bytes<kStagesShared>();
+  const LaunchChoice lc = num_ctas > 0 ? choose_launch(num_ctas, true) : choose_launch(auto_ctas(num_seqs, max_context), false);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(lc.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = lc.smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
+  if (lc.cluster > 1) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = unsigned(lc.cluster);
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
   if (flags & PKV_OVERLAP_PREVIOUS) {
     // programmatic stream serialization: the kernel may start while the previous kernel on
     // the stream finishes (see griddep_launch_dependents / griddep_wait in the kernel)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(G));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, a) != cudaSuccess) {
-      cudaGetLastError();
-      return PKV_ERR_LAUNCH;
-    }
-    return PKV_OK;
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
   }
-  kernel<<<G, kThreads, smem, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_LAUNCH;
+  cfg.attrs = attr;
+  cfg.numAttrs = unsigned(n_attr);
+  if (cudaLaunchKernelEx(&cfg, lc.kernel, a) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_LAUNCH;
+  }
   return PKV_OK;
 }
 
@@ -823,7 +1049,7 @@ extern "C" int pkv_decode_max_ctas(void) { return pkv::kMaxCtas; }
 
 extern "C" int pkv_decode_plan(int num_seqs, int max_context, int *num_ctas, int *launches) {
   if (num_seqs < 0 || max_context < 0) return PKV_ERR_SHAPE;
-  const int g = num_seqs == 0 ? 0 : pkv::auto_ctas(num_seqs, max_context);
+  const int g = num_seqs == 0 ? 0 : pkv::choose_launch(pkv::auto_ctas(num_seqs, max_context), false).grid;
   if (num_ctas) *num_ctas = g;
   if (launches) *launches = num_seqs == 0 ? 0 : 1;
   return PKV_OK;
