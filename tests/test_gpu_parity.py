@@ -174,6 +174,38 @@ def test_empty_and_invalid_contexts():
     U.assert_close(out[[1, 3, 5]], ref[[1, 3, 5]], "edge")
 
 
+def test_batch_without_pages_gives_zero_rows():
+    # no sequence has a page (contexts 0, or invalid): no CTA walks pages, every row is zero
+    for lens, status in (([0, 0, 0], 0), ([0, -5, 3000], 2)):
+        wl = configs.custom(452, lens, num_pages=4, name="nopages")
+        d = U.DeviceDecode(wl)
+        d.out.fill_(7.0)
+        out = d.attend(max_context=2048).cpu().double().numpy()
+        assert not out.any()
+        assert d.status_value() == status
+
+
+# Grids small enough for clusters of 8 (one CTA per SM) merge a cut sequence's parts on chip,
+# and only sequences cut across clusters meet in the workspace.  These splits put a
+# sequence's parts in one cluster (2 .. 8 CTAs: every receive-slot layout), across two or
+# more clusters (level-two tickets), and a single part in a cluster at either end.
+@pytest.mark.parametrize("lens,num_ctas", [
+    ([2048], 2), ([2048], 5), ([2048], 7), ([2048], 8), ([2048], 9), ([2048], 17), ([2048], 63),
+    ([2048], 120), ([128, 512, 1024, 2048], 58), ([128, 512, 1024, 2048], 0), ([300, 7, 1500, 40, 900], 13),
+    ([300, 7, 1500, 40, 900], 0), ([16] * 40 + [2048], 33)])
+def test_cluster_merge_layouts(lens, num_ctas):
+    wl = configs.custom(455, lens, spike_prob=0.01, name=f"clusters-{len(lens)}-{num_ctas}")
+    _check_workload(wl, num_ctas=num_ctas)
+
+
+def test_small_grids_launch_in_whole_clusters():
+    import paged_kv_cache_180_gb300 as pkv
+    g, _ = pkv.decode_plan(4, 2048)   # the Llama-shaped batch: a grid of whole 8-CTA clusters
+    assert g % 8 == 0 and 8 <= g <= 152
+    g, _ = pkv.decode_plan(256, 2048)  # a large batch: two CTAs per SM, no clusters
+    assert g > 152
+
+
 def test_invalid_page_sets_status_and_stays_finite():
     wl = configs.custom(460, [48, 20], name="badpage")
     d = U.DeviceDecode(wl)
