@@ -317,16 +317,28 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
                : "memory");
 }
 
-// ---- packed fp32 pairs and the hardware base-2 exponential ----
-// (x - m) * c on both halves of a pair, one packed subtract and one packed multiply.
-__device__ __forceinline__ float2 sub_mul_f32x2(float2 x, float2 m, float2 c) {
+// ---- packed fp32 pairs, three-input max / min, and the hardware base-2 exponential ----
+// a * b + c on both halves of a pair, one packed fused multiply-add.
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
   float2 r;
-  asm("{\n\t.reg .b64 xa, ma, ca, d;\n\t"
-      "mov.b64 xa, {%2, %3};\n\tmov.b64 ma, {%4, %5};\n\tmov.b64 ca, {%6, %7};\n\t"
-      "sub.rn.f32x2 d, xa, ma;\n\tmul.rn.f32x2 d, d, ca;\n\tmov.b64 {%0, %1}, d;\n\t}"
+  asm("{\n\t.reg .b64 aa, ba, ca, d;\n\t"
+      "mov.b64 aa, {%2, %3};\n\tmov.b64 ba, {%4, %5};\n\tmov.b64 ca, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, aa, ba, ca;\n\tmov.b64 {%0, %1}, d;\n\t}"
       : "=f"(r.x), "=f"(r.y)
-      : "f"(x.x), "f"(x.y), "f"(m.x), "f"(m.y), "f"(c.x), "f"(c.y));
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float2 sub_f32x2(float2 x, float2 y) {

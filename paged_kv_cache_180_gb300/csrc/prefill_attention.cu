@@ -158,17 +158,25 @@ __device__ __forceinline__ bool pf_wait(PfSmem &sm, uint64_t *bar, uint32_t pari
   return false;
 }
 
-// Largest (kMin: smallest) of 64 values, as a tree so the chain is 6 deep.
+template <bool kMin>
+__device__ __forceinline__ float ext3(float a, float b, float c) {
+  return kMin ? min3f(a, b, c) : max3f(a, b, c);
+}
+
+// Largest (kMin: smallest) of 64 values: a tree of three-input max (32 instructions, 4 deep).
 template <bool kMin>
 __device__ __forceinline__ float extreme64(const float (&x)[64]) {
-  float m[32];
+  float m[22];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) m[c] = kMin ? fminf(x[c], x[c + 32]) : fmaxf(x[c], x[c + 32]);
+  for (int i = 0; i < 21; ++i) m[i] = ext3<kMin>(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  m[21] = x[63];
+  float n[8];
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int c = 0; c < w; ++c) m[c] = kMin ? fminf(m[c], m[c + w]) : fmaxf(m[c], m[c + w]);
-  return m[0];
+  for (int i = 0; i < 7; ++i) n[i] = ext3<kMin>(m[3 * i], m[3 * i + 1], m[3 * i + 2]);
+  n[7] = m[21];
+  const float a = ext3<kMin>(n[0], n[1], n[2]), b = ext3<kMin>(n[3], n[4], n[5]);
+  const float c = kMin ? fminf(n[6], n[7]) : fmaxf(n[6], n[7]);
+  return ext3<kMin>(a, b, c);
 }
 
 // max over the keys whose bit in `valid` is set of sigma * s, sigma = -1 when neg.
@@ -186,10 +194,11 @@ __device__ __forceinline__ float signed_max(const float (&sv)[64], bool masked, 
 template <bool kMasked>
 __device__ __forceinline__ void block_probs(const float (&sv)[64], uint64_t valid, float m, float2 c2,
                                             uint32_t (&hi)[32], uint32_t (&lo)[32]) {
-  const float2 m2 = make_float2(m, m);
+  // exponent arguments (s - m) c as one packed fused multiply-add: s c + (-m c)
+  const float2 mc = make_float2(-m * c2.x, -m * c2.y);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float2 e = sub_mul_f32x2(make_float2(sv[2 * i], sv[2 * i + 1]), m2, c2);
+    const float2 e = fma_f32x2(make_float2(sv[2 * i], sv[2 * i + 1]), c2, mc);
     float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
     if (kMasked) {
       p0 = (valid >> (2 * i)) & 1 ? p0 : 0.f;
