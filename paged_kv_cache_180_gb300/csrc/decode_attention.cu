@@ -316,20 +316,21 @@ __device__ __forceinline__ int ticket_of(const DecodeArgs &a, int s, long long g
 
 // Merge of `count` partial states for this lane's query head h and dims d0 .. d0 + 7:
 // the running maximum M, sum L and accumulator r.  read(k, ml, x0, x1) loads part k's
-// (m, l) and accumulator dims d0 .. d0 + 7.  The parts are read kMergeBatch at a time,
-// every load of a batch issued before the first is used, so a batch costs one round
-// trip; the batch's maximum rescales the running state once.
-template <class Read>
+// (m, l) and accumulator dims d0 .. d0 + 7.  The parts are read kBatch at a time, every
+// load of a batch issued before the first is used, so a batch costs one round trip; the
+// batch's maximum rescales the running state once.  (Eight at a time where the warp has
+// the registers to spare: the clusters' states after the page loop.)
+template <int kBatch = kMergeBatch, class Read>
 __device__ __forceinline__ void merge_states(int count, Read read, float &M, float &L, float (&r)[8]) {
   M = -INFINITY;
   L = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) r[i] = 0.f;
-  for (int k0 = 0; k0 < count; k0 += kMergeBatch) {
-    float2 ml[kMergeBatch];
-    float4 x0[kMergeBatch], x1[kMergeBatch];
+  for (int k0 = 0; k0 < count; k0 += kBatch) {
+    float2 ml[kBatch];
+    float4 x0[kBatch], x1[kBatch];
 #pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j) {
+    for (int j = 0; j < kBatch; ++j) {
       if (k0 + j < count) {
         read(k0 + j, ml[j], x0[j], x1[j]);
       } else {
@@ -340,13 +341,13 @@ __device__ __forceinline__ void merge_states(int count, Read read, float &M, flo
     // a part whose pages were all invalid (or a padding entry) has m = -inf and weight 0
     float m_new = M;
 #pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j) m_new = fmaxf(m_new, ml[j].x);
+    for (int j = 0; j < kBatch; ++j) m_new = fmaxf(m_new, ml[j].x);
     const float keep = (m_new == -INFINITY) ? 1.f : exp2f(M - m_new);
     L *= keep;
 #pragma unroll
     for (int i = 0; i < 8; ++i) r[i] *= keep;
 #pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j) {
+    for (int j = 0; j < kBatch; ++j) {
       const float wgt = (ml[j].x == -INFINITY) ? 0.f : exp2f(ml[j].x - m_new);
       L += ml[j].y * wgt;
       r[0] += wgt * x0[j].x; r[1] += wgt * x0[j].y; r[2] += wgt * x0[j].z; r[3] += wgt * x0[j].w;
@@ -486,7 +487,7 @@ __device__ __forceinline__ void cluster_merge(const DecodeArgs &a, const RecvAre
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __syncwarp();  // lane 0's acquire comes before every lane's reads of the clusters' states
-  merge_states(
+  merge_states<8>(
       k1 - k0 + 1,
       [&](int k, float2 &ml, float4 &x0, float4 &x1) {
         const Slot &part = a.slots[(long long)(k == 0 ? c.c_first : (k0 + k) * kClusterCtas) + s];
