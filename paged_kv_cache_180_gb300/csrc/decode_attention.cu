@@ -529,6 +529,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
     mbar_init_fence();
   }
 
+  // Small grids: the block-table entries are read right after the lengths, so start their
+  // lines toward L2 now, spread over the CTAs (each row's first ceil(max_context / 16)
+  // entries, and no byte outside them).  (Large grids measured no gain from it.)
+  if (kStages == kStagesAlone && tid < 4) {
+    const long long row_bytes = (long long)((a.max_context + kPageTokens - 1) / kPageTokens) * 4;
+    const long long per_row = (row_bytes + 127) / 128 + 1;
+    const long long idx = cta + (long long)tid * G;
+    if (row_bytes > 0 && idx < (long long)a.num_seqs * per_row) {
+      const long long s = idx / per_row, k = idx % per_row;
+      const long long off = k * 128 < row_bytes - 4 ? k * 128 : row_bytes - 4;
+      prefetch_l2(reinterpret_cast<const uint8_t *>(a.block_tables + s * a.bt_stride) + off);
+    }
+  }
+
   // ---- total pages T, and this CTA's range [pa, pb) ----
   // Per thread: pages, sequences with pages, and the least and most pages of one sequence.
   long long mine = 0;
