@@ -15,7 +15,8 @@
 //
 // GB300 design
 //  * Work split: the pages of all sequences form one list (sequence-major); the
-//    grid has G CTAs (2 per SM) and, from the lengths it reads on the device,
+//    grid has G CTAs (two per SM, or one per SM for small batches) and, from the
+//    lengths it reads on the device,
 //    the kernel picks how many of them (Gu) share the T pages: CTA c takes pages
 //    [c*T/Gu, (c+1)*T/Gu), so every CTA streams the same number of bytes
 //    whatever the mix of context lengths.  Equal-length batches are split along
@@ -30,7 +31,8 @@
 //    staircase; the ticket counters of s live in slot (first CTA of s) + s and
 //    are reset by the merging warps, so a zeroed workspace stays valid across
 //    calls of any batch size.  Sequences with no
-//    pages (context 0 or invalid) get zero rows from CTA s % G.
+//    pages (context 0 or invalid) get zero rows from CTA s % G.  Small grids
+//    start their block-table lines toward L2 at entry, as the lengths are read.
 //  * Small grids (no more CTAs than can be resident in clusters of 8 at one CTA
 //    per SM) are launched in thread-block clusters of 8 consecutive CTAs, and
 //    the first merge level stays on chip: the CTAs of a cluster that hold parts
