@@ -109,9 +109,9 @@ struct GroupState {
   float acc[kGroup][kHeadDim];  // un-normalised sum of p * V of query heads 4g .. 4g+3
   float2 ml[kGroup];            // (running max in log2 units, sum of p)
 };
-// A sequence held by p <= kClusterCtas CTAs of a cluster has its head group g merged by its
-// CTA g % p, which so receives p parts of at most ceil(kWarps / p) head groups: at most 14
-// (p = 7) states.
+// A sequence held by p <= kClusterCtas CTAs of a cluster has its head group g merged by the
+// (g mod p)-th of those CTAs, which so receives p parts of at most ceil(kWarps / p) head
+// groups: at most 14 states (p = 7).
 constexpr int kRecvSlots = 14;
 struct RecvArea {
   GroupState slot[kRecvSlots];  // slot k * ceil(kWarps / p) + g / p: part k, head group g
