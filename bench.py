@@ -23,6 +23,7 @@ slow baseline).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -740,6 +741,17 @@ def trace_host_steps(tr, steps: int) -> dict:
     t0 = time.perf_counter()
     plans = [sched.step() for _ in range(steps)]
     host_plan_us = (time.perf_counter() - t0) / steps * 1e6
+    # the same plans from a second scheduler through the bare C call (no copies into numpy
+    # arrays): the native scheduler's own cost per step
+    native = pkv.Scheduler(tr.num_pages, 1, 16, tr.max_context, tr.num_slots, tr.free_order)
+    for rid in range(tr.num_requests):
+        native.submit(rid, int(tr.prompt_lens[rid]), int(tr.new_budgets[rid]))
+    raw = pkv.binding.PkvStepPlan()
+    step_fn, handle = pkv.binding._lib.pkv_sched_step, native._h
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step_fn(handle, ctypes.byref(raw))
+    native_plan_us = (time.perf_counter() - t0) / steps * 1e6
     host_steps, bytes_per_step = [], []
     attn_bytes = app_bytes = seq_layers = 0
     for i, pl in enumerate(plans):
@@ -785,6 +797,7 @@ def trace_host_steps(tr, steps: int) -> dict:
         seq_layers += int(live.sum())
     return {"host_steps": host_steps, "bytes_per_step": bytes_per_step, "attn_bytes": attn_bytes,
             "app_bytes": app_bytes, "seq_layers": seq_layers, "host_plan_us": round(host_plan_us, 2),
+            "native_plan_us": round(native_plan_us, 2),
             "stats": sched.stats()}
 
 
@@ -852,7 +865,8 @@ def trace_measure(args, dev, steps: int, warmup: int, world: int, sampler, with_
                                 "launch-bound"},
            "algorithmic_bytes": attn_bytes + app_bytes,
            "seq_layers_per_s": round(world * seq_layers / (total_ms * 1e-3), 1),
-           "host_plan_us_per_step": plan["host_plan_us"], "scheduler_stats": plan["stats"],
+           "host_plan_us_per_step": plan["host_plan_us"], "native_plan_us_per_step": plan["native_plan_us"],
+           "scheduler_stats": plan["stats"],
            "clocks": sampler.summary(tw0, tw1),
            "gpu_launches": sum((1 if x["k_prompt"] is not None else 0) + 1 for x in per_step),
            "_total_ms": total_ms, "_gbs": gbs}
@@ -1120,7 +1134,8 @@ def run_trace(args):
                 "dtype": "bf16 in, f32 accumulate/out", "data": "synthetic (seeded N(0,1) bf16; seeded request trace)",
                 "config": {k: rec[k] for k in ("workload", "slots", "layers", "pool_pages", "requests", "prompt",
                                                "new_tokens", "l2", "timing")} | {"parallelism": f"replicas x{world}"},
-                **{k: rec[k] for k in ("roofline", "seq_layers_per_s", "host_plan_us_per_step", "scheduler_stats",
+                **{k: rec[k] for k in ("roofline", "seq_layers_per_s", "host_plan_us_per_step",
+                                       "native_plan_us_per_step", "scheduler_stats",
                                        "clocks", "gpu_launches") if k in rec}}
         if "cpu_baseline" in rec:
             line["cpu_baseline"] = rec["cpu_baseline"]
