@@ -14,8 +14,9 @@
 // GB300 design (tcgen05 tensor cores, accumulators in tensor memory)
 //  * Tile: 32 query tokens of a sequence against one K/V head g.  Its 128 rows
 //    (row = 4 * token + head in group) share every K/V row loaded: M = 128.  The
-//    grid is persistent (two CTAs per SM); each CTA walks the tiles blockIdx.x,
-//    + gridDim.x, ..., numbered latest-first so the longest causal spans start first.
+//    grid is persistent (two CTAs per SM); the tiles are numbered latest-first (the
+//    longest causal spans start first) and dealt to the CTAs in a snake, forward on even
+//    rounds and backward on odd ones, which evens out the CTAs' key blocks.
 //  * Keys in blocks of 64 (4 pages).  S = Q K^T is 4 tcgen05.mma (M 128, N 64,
 //    K 16; Q and K K-major, 128-byte swizzled) into one of two TMEM S buffers, so
 //    S of block j + 1 runs while the softmax works on block j.  P, as bf16 hi + lo
@@ -210,7 +211,7 @@ __device__ __forceinline__ void block_probs(const float (&sv)[64], uint64_t vali
   }
 }
 
-// Persistent: each CTA walks the tiles blockIdx.x, + gridDim.x, ... (at most kPfMaxTiles;
+// Persistent: each CTA walks its tiles of the snake order (at most kPfMaxTiles;
 // their descriptors are read from global memory once, in parallel, into shared memory).
 // Every role walks the same table and skips the same tiles, so their running block
 // counters agree.  The loader fetches the next tile's Q and block-table entries while the
@@ -221,9 +222,14 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) paged_prefill_kernel
   extern __shared__ uint8_t smem_raw[];
   PfSmem &sm = *reinterpret_cast<PfSmem *>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nt = (a.num_tiles - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);  // <= kPfMaxTiles
+  // Tile k of this CTA: k * G + c on even rounds and k * G + (G - 1 - c) on odd ones, a snake
+  // over the latest-first list that evens out the CTAs' key blocks.
+  const int G = int(gridDim.x), c = int(blockIdx.x);
+  auto tile_index = [&](int k) { return k * G + ((k & 1) ? G - 1 - c : c); };
+  int nt = 0;  // <= kPfMaxTiles
+  while (nt < kPfMaxTiles && tile_index(nt) < a.num_tiles) ++nt;
 
-  if (tid < nt) sm.tiles[tid] = pf_tile(a, int(blockIdx.x) + tid * int(gridDim.x));
+  if (tid < nt) sm.tiles[tid] = pf_tile(a, tile_index(tid));
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 1);
