@@ -32,7 +32,8 @@
 //    are reset by the merging warps, so a zeroed workspace stays valid across
 //    calls of any batch size.  Sequences with no
 //    pages (context 0 or invalid) get zero rows from CTA s % G.  Small grids
-//    start their block-table lines toward L2 at entry, as the lengths are read.
+//    start their block-table and query lines toward L2 at entry, as the lengths
+//    are read.
 //  * Small grids (no more CTAs than can be resident in clusters of 8 at one CTA
 //    per SM) are launched in thread-block clusters of 8 consecutive CTAs, and
 //    the first merge level stays on chip: the CTAs of a cluster that hold parts
@@ -543,6 +544,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_decode_partial_ker
       const long long off = k * 128 < row_bytes - 4 ? k * 128 : row_bytes - 4;
       prefetch_l2(reinterpret_cast<const uint8_t *>(a.block_tables + s * a.bt_stride) + off);
     }
+  }
+
+  // ... and the query rows, read right after griddep_wait: a prefetch into L2 brings nothing
+  // into this SM, so those loads still see whatever the kernel before this one wrote.
+  if (kStages == kStagesAlone && tid >= 32 && tid < 40) {
+    const long long idx = cta + (long long)(tid - 32) * G;  // 128-byte lines, 32 per sequence
+    if (idx < (long long)a.num_seqs * (kQHeads * kHeadDim * 2 / 128))
+      prefetch_l2(reinterpret_cast<const uint8_t *>(a.q) + idx * 128);
   }
 
   // ---- total pages T, and this CTA's range [pa, pb) ----
