@@ -1,5 +1,7 @@
-"""bench.py's roofline `traffic` comes from a committed ncu record only when that record was
-taken on the current kernel source and on the same workload (no GPU needed)."""
+"""bench.py's host-side records, no GPU needed: the roofline `traffic` comes from a committed
+ncu record only when that record was taken on the current kernel source and on the same
+workload, and the `clocks` summary keeps the nvidia-smi samples of the timed region (or the
+nearest one) with their throttle reasons."""
 import hashlib
 import json
 import os
@@ -32,3 +34,32 @@ def test_nvtx_ranges_are_off_by_default():
     assert bench.NVTX is False
     with bench.nvtx("anything"):
         pass
+
+
+def _smi_line(sm, mx, power, hw="Not Active", thermal="Not Active", sw_thermal="Not Active", cap="Not Active"):
+    # the fields of ClockSampler.QUERY, in order, as nvidia-smi prints them (csv, no units)
+    return f"2026/01/01 00:00:00.000, 0, {sm}, {mx}, {power}, 0x0000000000000000, {hw}, {thermal}, {sw_thermal}, {cap}"
+
+
+def test_clock_summary_takes_the_samples_inside_the_timed_region():
+    s = bench.ClockSampler(0)
+    s.lines = [(9.0, _smi_line(1000, 2070, 100.0, hw="Active")),      # before the region: ignored
+               (10.0, _smi_line(2070, 2070, 600.0)),
+               (10.1, _smi_line(2040, 2070, 700.0, cap="Active")),
+               (10.2, _smi_line(2055, 2070, 650.0)),
+               (12.0, _smi_line(500, 2070, 90.0, thermal="Active"))]  # after it: ignored
+    out = s.summary(10.0, 10.2)
+    assert out["samples"] == 3
+    assert out["sm_mhz"] == 2055.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w_max"] == 700.0
+
+
+def test_clock_summary_reports_slowdowns_and_falls_back_to_the_nearest_sample():
+    s = bench.ClockSampler(0)
+    s.lines = [(5.0, _smi_line(1500, 2070, 300.0, hw="Active", sw_thermal="Active")), (7.0, "garbled line")]
+    inside = s.summary(5.0, 5.001)
+    assert inside["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and inside["samples"] == 1
+    near = s.summary(5.2, 5.203)  # shorter than the sampling period, no sample inside
+    assert near["samples"] == 1 and near["sm_mhz"] == 1500.0 and "note" in near
+    assert bench.ClockSampler(0).summary(0.0, 1.0)["samples"] == 0
