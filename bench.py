@@ -68,6 +68,9 @@ def parse_args():
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step as a CUDA graph (auto: on for the launch-bound workloads)")
     p.add_argument("--nvtx", action="store_true", help="NVTX ranges around the bench phases and steps")
+    p.add_argument("--prefill-shape", default="16,512", metavar="SEQS,TOKENS",
+                   help="prompts of the prefill workload (default 16 x 512; another shape is reported under "
+                        "its own workload name, e.g. prefill_4x2048)")
     p.add_argument("--overlap", choices=["auto", "on", "off"], default="auto",
                    help="launch each layer's fused step with PKV_OVERLAP_PREVIOUS, so it starts while the "
                         "previous layer's finishes (auto: on for multi-layer fused steps)")
@@ -877,8 +880,16 @@ def trace_measure(args, dev, steps: int, warmup: int, world: int, sampler, with_
     return rec
 
 
+def prefill_shape(args) -> tuple[int, int, str]:
+    """(sequences, prompt tokens, workload name) of the prefill workload: 16 x 512 is "prefill"."""
+    nseq, plen = (int(x) for x in str(getattr(args, "prefill_shape", "16,512")).split(","))
+    if not (nseq >= 1 and 1 <= plen <= 2048):
+        raise SystemExit("--prefill-shape wants SEQS >= 1 and 1 <= TOKENS <= 2048")
+    return nseq, plen, "prefill" if (nseq, plen) == (16, 512) else f"prefill_{nseq}x{plen}"
+
+
 def prefill_measure(args, dev, steps: int, warmup: int, world: int, sampler, with_cpu: bool):
-    """Paged prefill: 16 sequences x 512-token prompts (the pages' longest prompt), 1 layer.
+    """Paged prefill: 16 sequences x 512-token prompts (the pages' longest prompt) by default, 1 layer.
     A step appends every prompt token (kv_append) and runs causal paged prefill attention.
     Tensor-bound: the roofline counts the causal flops, 4 * head_dim * q_heads * sum_i (p_i + 1)
     (QK^T and PV, 2 flops per multiply-add), against the measured bf16 tensor peak."""
@@ -887,7 +898,7 @@ def prefill_measure(args, dev, steps: int, warmup: int, world: int, sampler, wit
     import paged_kv_cache_180_gb300 as pkv
     from workloads import configs, rng, torch_gen
 
-    nseq, plen = 16, 512
+    nseq, plen, label = prefill_shape(args)
     wl = configs.custom(187, [plen] * nseq, name="prefill")
     pool = pkv.KVPool(wl.num_pages, device=dev)
     k, v, slots = torch_gen.workload_kv(wl, 0, dev)
@@ -969,7 +980,7 @@ def prefill_measure(args, dev, steps: int, warmup: int, world: int, sampler, wit
     att_s = sum(att_ms) / steps * 1e-3
     tflops = flops / att_s / 1e12
     peak, peak_kind = measured_tensor_peak()
-    rec = {"workload": "prefill", "num_seqs": nseq, "prompt_tokens": plen, "layers": 1, "steps": steps,
+    rec = {"workload": label, "num_seqs": nseq, "prompt_tokens": plen, "layers": 1, "steps": steps,
            "warmup": warmup, "overlap_previous": bool(overlap), "l2": "flushed between steps",
            "timing": ("CUDA graph replay per step (whole step; attention-only graph for the per-kernel figure)"
                       if graphs is not None else "CUDA events around each kernel"),
@@ -978,7 +989,7 @@ def prefill_measure(args, dev, steps: int, warmup: int, world: int, sampler, wit
            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                         "frac": round(tflops / peak, 4),
                         "traffic": committed_traffic("prefill_attention_traffic.json", "prefill_attention.cu",
-                                                     wl.name),
+                                                     label),
                         "algorithmic_flops_per_launch": flops, "avg_launch_us": round(att_s * 1e6, 3),
                         "peak_source": (f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json, cuBLAS burst)"
                                         if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},
