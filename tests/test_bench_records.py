@@ -63,3 +63,12 @@ def test_clock_summary_reports_slowdowns_and_falls_back_to_the_nearest_sample():
     near = s.summary(5.2, 5.203)  # shorter than the sampling period, no sample inside
     assert near["samples"] == 1 and near["sm_mhz"] == 1500.0 and "note" in near
     assert bench.ClockSampler(0).summary(0.0, 1.0)["samples"] == 0
+
+
+def test_prefill_shape_option_names_its_workload():
+    import types
+    assert bench.prefill_shape(types.SimpleNamespace(prefill_shape="16,512")) == (16, 512, "prefill")
+    assert bench.prefill_shape(types.SimpleNamespace(prefill_shape="4,2048")) == (4, 2048, "prefill_4x2048")
+    assert bench.prefill_shape(types.SimpleNamespace()) == (16, 512, "prefill")
+    # a shape other than the recorded one never picks up the committed traffic record
+    assert bench.committed_traffic("prefill_attention_traffic.json", "prefill_attention.cu", "prefill_4x2048") is None
