@@ -490,6 +490,45 @@ def test_overlapped_steps_sharing_output_and_workspace():
     assert torch.equal(d.out, copies[L - 1])
 
 
+def test_overlapped_step_reads_q_written_by_the_kernel_before():
+    """A small batch (the clustered instance, which starts its query lines toward L2 before it
+    waits for the kernel before it) launched with overlap_previous right after a kv_append
+    that writes the very bytes it then reads as q: the K half of a spare page, 16 appended
+    tokens of 8 heads, is the 4 x 32 x 64 query block.  The outputs must match the oracle fed
+    with the bytes of its own append, on every repetition (new values each time)."""
+    import paged_kv_cache_180_gb300 as pkv
+    from workloads import torch_gen
+    lens = [128, 512, 1024, 2048]
+    need = sum(-(-c // 16) for c in lens)
+    wl = configs.custom(191, lens, num_pages=need + 64, name="q-written-before")
+    used = set(int(x) for x in wl.block_tables[:, 0, :].reshape(-1) if x >= 0)
+    spare = [pg for pg in range(wl.num_pages) if pg not in used]
+    assert len(spare) == 64
+    qpage = spare[0]
+    d = U.DeviceDecode(wl)
+    k, v, slots = torch_gen.workload_kv(wl, 0, U.dev(), upto_offset=1)
+    pkv.kv_append(d.pool, k, v, slots, d.status)
+    kn, vn, sn = (U.to_dev(a) for a in wl.decode_tokens(0))
+    q_dev = d.pool.view()[qpage, 0].view(4, 32, 64)  # the spare page's K half itself, read as q
+    _, err, opool = oracle.decode_workload(wl)
+    assert err == 0
+    spare_slots = np.array([pg * 16 + r for pg in spare for r in range(16)], dtype=np.int32)
+    n = spare_slots.size * 8 * 64
+    bt0 = np.ascontiguousarray(wl.block_tables[:, 0, :])
+    for rep in range(6):
+        ks = rng.normal_bf16(rng.stream_key(191, f"spare-k-{rep}"), 0, n).reshape(-1, 8, 64)
+        vs = rng.normal_bf16(rng.stream_key(191, f"spare-v-{rep}"), 0, n).reshape(-1, 8, 64)
+        pkv.kv_append(d.pool, U.to_dev(ks), U.to_dev(vs), U.to_dev(spare_slots), d.status)
+        pkv.decode_step(d.pool, kn, vn, sn, d.out, q_dev, d.bt.view(-1), wl.max_blocks, d.lens, wl.max_context,
+                        wl.scale, d.ws, d.status, overlap_previous=True)
+        assert d.status_value() == 0
+        assert oracle.kv_append(opool, ks, vs, spare_slots) == 0
+        q_host = np.ascontiguousarray(opool.data[qpage, 0]).reshape(4, 32, 64)
+        ref, err = oracle.paged_decode_attention(opool, q_host, bt0, wl.context_lens, wl.scale, wl.max_context)
+        assert err == 0
+        U.assert_close(d.out.cpu().double().numpy(), ref, f"q written by the append before, repetition {rep}")
+
+
 @pytest.mark.parametrize("pad", [0, 256], ids=["packed", "padded_stride"])
 def test_separate_k_and_v_buffers(pad):
     """K and V pools in two separate allocations with a page stride of half a page (plus
